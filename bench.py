@@ -1,0 +1,487 @@
+"""Benchmark of the MXFP8 norm-quant + GEMM hot path on GB300.
+
+One step = one pass of the whole path over one batch of M tokens:
+  1. fused Gemma RMSNorm + MXFP8 quantisation of the residual x (M x 6144),
+  2. MXFP8 quantisation of the o_proj activation A (M x 2048) and its GEMM
+     against the pre-quantised weight W (6144 x 2048), bf16 out,
+  3. the same for the down_proj activation (M x 3072) and W (6144 x 3072).
+Weights are quantised once, before timing (serving loads MXFP8 weights).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload m1024]
+    python bench.py --impl reference ...   # the CPU oracle, timed on a bounded sample
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs the same
+per-GPU workload on its own batch (weak scaling, no collective on the data
+path); the barrier-bracketed time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H = 6144
+N_OUT = 6144
+EPS = 1e-6
+L2_BYTES = 129 * 1024 * 1024
+FP8_PER_BF16 = 2.0        # dense FP8 / dense BF16 tensor rate (4.5 / 2.25 PFLOP/s nominal)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ traffic model
+
+def norm_quant_bytes(m, h=H):
+    """Algorithmic HBM bytes of one fused norm-quant launch: read x (2 B/elem),
+    write codes (1 B/elem) and scales (padded F8_128x4 buffer), read w once."""
+    c = h // 32
+    scale = (-(-m // 128) * 128) * (-(-c // 4) * 4)
+    return 2 * m * h + m * h + scale + 2 * h
+
+
+def quant_bytes(r, c):
+    cs = c // 32
+    return 2 * r * c + r * c + (-(-r // 128) * 128) * (-(-cs // 4) * 4)
+
+
+def gemm_flops(m, n, k):
+    return 2.0 * m * n * k
+
+
+def gemm_bytes(m, n, k):
+    sa = (-(-m // 128) * 128) * (k // 32)
+    sb = (-(-n // 128) * 128) * (k // 32)
+    return m * k + sa + n * k + sb + 2 * m * n
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import mxfp8_norm_quant_gb300 as mx
+    from mxfp8_norm_quant_gb300 import workloads as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mx.lib()
+    wl = W.WORKLOADS[args.workload]
+    M = wl.m
+    ks = wl.ks
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+
+    # ---- inputs, resident in HBM; R rotating sets so that the working set of
+    # consecutive steps exceeds L2 (no flush needed between steps)
+    x_h, w_h = wl.norm(seed=rank)
+    a_h = {k: wl.gemm(k, seed=rank)[0] for k in ks}
+    wt_h = {k: wl.gemm(k, seed=rank)[1] for k in ks}
+    w_dev = w_h.to(dev)
+    wq = {}
+    for k in ks:
+        wd = wt_h[k].to(dev)
+        wq[k] = mx.quant(wd)
+        del wd
+    set_bytes = 2 * M * H + M * H + mx.mx_scale_bytes(M, H)
+    for k in ks:
+        set_bytes += 3 * M * k + mx.mx_scale_bytes(M, k) + 2 * M * N_OUT
+    weight_bytes = sum(N_OUT * k + mx.mx_scale_bytes(N_OUT, k) for k in ks)
+    R = max(2, math.ceil(2.2 * L2_BYTES / max(1, set_bytes + weight_bytes)))
+    R = min(R, 16)
+    sets = []
+    for r in range(R):
+        s = {"x": x_h.to(dev), "q": torch.empty((M, H), dtype=torch.uint8, device=dev),
+             "s": torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)}
+        for k in ks:
+            s[f"a{k}"] = a_h[k].to(dev)
+            s[f"aq{k}"] = torch.empty((M, k), dtype=torch.uint8, device=dev)
+            s[f"as{k}"] = torch.empty(mx.mx_scale_bytes(M, k), dtype=torch.uint8, device=dev)
+            s[f"c{k}"] = torch.empty((M, N_OUT), dtype=torch.bfloat16, device=dev)
+        sets.append(s)
+    # weights rotate too (each decoder layer has its own)
+    wsets = [wq] + [{k: (wq[k][0].clone(), wq[k][1].clone()) for k in ks} for _ in range(R - 1)]
+    torch.cuda.synchronize()
+
+    kernels = ["norm_quant"] + [f"quant_a{k}" for k in ks] + [f"gemm_k{k}" for k in ks]
+
+    def step(i, ev=None):
+        s = sets[i % R]
+        wsx = wsets[i % R]
+        j = 0
+
+        def mark():
+            nonlocal j
+            if ev is not None:
+                ev[j].record(stream)
+            j += 1
+
+        mark()
+        mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], M, H, sptr)
+        mark()
+        for k in ks:
+            mx.mx_quant_weights(s[f"a{k}"], s[f"aq{k}"], s[f"as{k}"], M, k, sptr)
+            mark()
+            mx.mx_gemm(s[f"aq{k}"], s[f"as{k}"], wsx[k][0], wsx[k][1], s[f"c{k}"], M, N_OUT, k, sptr)
+            mark()
+
+    n_marks = 2 + 2 * len(ks)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    assert mx.mx_device_fault() == 0
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    # soak ~1.5 s so the clocks under load are sampled and settled
+    t_soak = time.time()
+    i = 0
+    with torch.cuda.stream(stream):
+        while time.time() - t_soak < 1.5:
+            for _ in range(50):
+                step(i)
+                i += 1
+            stream.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(i, evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    assert mx.mx_device_fault() == 0
+
+    total_ms = evs[0][0].elapsed_time(evs[-1][n_marks - 1])
+    per_kernel = {name: 0.0 for name in kernels}
+    order = ["norm_quant"]
+    for k in ks:
+        order += [f"quant_a{k}", f"gemm_k{k}"]
+    for e in evs:
+        for idx, name in enumerate(order):
+            per_kernel[name] += e[idx].elapsed_time(e[idx + 1])
+    ms_per_step = total_ms / args.steps
+
+    flops_step = sum(gemm_flops(M, N_OUT, k) for k in ks)
+    gemm_ms = sum(per_kernel[f"gemm_k{k}"] for k in ks)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks)
+
+    # ---- aggregate over ranks: max time, sum of work
+    times = [ms_per_step]
+    if world > 1:
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        times = [float(t.item())]
+    ms_max = times[0]
+    value = world * flops_step / (ms_max * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    gemm_tflops = flops_step * args.steps / (gemm_ms * 1e-3) / 1e12
+    nq_ms = per_kernel["norm_quant"] / args.steps
+    nq_gbs = norm_quant_bytes(M) / (nq_ms * 1e-3) / 1e9
+    kern = {}
+    for name in order:
+        ms = per_kernel[name] / args.steps
+        if name == "norm_quant":
+            b = norm_quant_bytes(M)
+            kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
+                          peaks["hbm_gbs"], "share": per_kernel[name] / total_ms}
+        elif name.startswith("quant_a"):
+            k = int(name[7:])
+            b = quant_bytes(M, k)
+            kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
+                          peaks["hbm_gbs"], "share": per_kernel[name] / total_ms}
+        else:
+            k = int(name[6:])
+            f = gemm_flops(M, N_OUT, k)
+            kern[name] = {"us": ms * 1e3, "TFLOP/s": f / (ms * 1e-3) / 1e12,
+                          "frac_fp8": f / (ms * 1e-3) / 1e12 / fp8_peak, "share": per_kernel[name] / total_ms}
+    plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
+
+    clocks = sampler.summary(t_soak, t_wall1)
+    out = {
+        "metric": "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3+ue8m0 in, fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, U(-0.1,0.1) norm gain)",
+        "config": {"workload": wl.name, "M": M, "N": N_OUT, "K": list(ks), "norm_quant": f"{M}x{H}",
+                   "step": "norm-quant(x) + per K: quant(A) + gemm(A, W_pre-quantised)",
+                   "l2": f"{R} rotating input+weight sets, {(set_bytes + weight_bytes) * R / 2**20:.0f} MiB "
+                         f"total > L2 (no flush)",
+                   "parallelism": f"weak, {world} independent rank(s)", "gemm_plan": plan},
+        "gemm_tflops": gemm_tflops,
+        "norm_quant_gbs": nq_gbs,
+        "kernels": kern,
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / fp8_peak, "traffic": None,
+                     "kernel": "k_gemm_mxf8 (both launches of the step)",
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_PER_BF16} "
+                                    "(nominal dense FP8/BF16 ratio)"},
+        "norm_quant_roofline": {"bound": "hbm", "achieved": nq_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": nq_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
+        "e2e": e2e,
+        "gpu_launches": len(order) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(wl, ks, budget_s=args.cpu_seconds)
+    return out
+
+
+def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
+    """Same metric end to end: pinned host inputs -> device, the step, outputs -> host."""
+    M = wl.m
+    x_pin = x_h.pin_memory()
+    a_pin = {k: a_h[k].pin_memory() for k in ks}
+    xd = torch.empty_like(x_pin, device=dev)
+    ad = {k: torch.empty_like(a_pin[k], device=dev) for k in ks}
+    q = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    s = torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)
+    aq = {k: torch.empty((M, k), dtype=torch.uint8, device=dev) for k in ks}
+    as_ = {k: torch.empty(mx.mx_scale_bytes(M, k), dtype=torch.uint8, device=dev) for k in ks}
+    c = {k: torch.empty((M, N_OUT), dtype=torch.bfloat16, device=dev) for k in ks}
+    q_h = torch.empty_like(q, device="cpu").pin_memory()
+    s_h = torch.empty_like(s, device="cpu").pin_memory()
+    c_h = {k: torch.empty_like(c[k], device="cpu").pin_memory() for k in ks}
+    h2d = x_pin.numel() * 2 + sum(a_pin[k].numel() * 2 for k in ks)
+    d2h = q.numel() + s.numel() + sum(c[k].numel() * 2 for k in ks)
+    sptr = stream.cuda_stream
+
+    def step():
+        xd.copy_(x_pin, non_blocking=True)
+        mx.mx_rmsnorm_quant(xd, w_dev, EPS, q, s, M, H, sptr)
+        for k in ks:
+            ad[k].copy_(a_pin[k], non_blocking=True)
+            mx.mx_quant_weights(ad[k], aq[k], as_[k], M, k, sptr)
+            mx.mx_gemm(aq[k], as_[k], wq[k][0], wq[k][1], c[k], M, N_OUT, k, sptr)
+        q_h.copy_(q, non_blocking=True)
+        s_h.copy_(s, non_blocking=True)
+        for k in ks:
+            c_h[k].copy_(c[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = sum(gemm_flops(M, N_OUT, k) for k in ks)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, ks, budget_s=15.0, rows=16):
+    """The oracle as it stands, on a bounded row sample of one step: norm-quant of
+    `rows` rows of x, quantisation of `rows` rows of each A, and their GEMM rows
+    against the full weight (quantised and decoded by the oracle).  Repeated
+    until budget_s of CPU time; scaled to TFLOP/s of GEMM work."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x, w = wl.norm(seed=0)
+    xs = bits(x[:rows])
+    wb = bits(w)
+    ops = []
+    for k in ks:
+        a, wt = wl.gemm(k, seed=0)
+        bq, bs = O.quant(bits(wt))
+        ops.append((k, bits(a[:rows]), bq, bs))
+    flops = 0.0
+    t0 = time.time()
+    n = 0
+    while True:
+        O.rmsnorm_quant(xs, wb, EPS)
+        for k, ab, bq, bs in ops:
+            aq, as_ = O.quant(ab)
+            O.gemm_ref(aq, as_, bq, bs)
+            flops += gemm_flops(rows, N_OUT, k)
+        n += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"{n} x ({rows} rows of norm-quant {wl.m}x{H}; {rows} rows of quant + GEMM vs the full "
+                      f"6144-row weight for K={list(ks)}), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    from mxfp8_norm_quant_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    ks = wl.ks
+    budget = max(2.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, ks, budget_s=0.0, rows=8)
+    t0 = time.time()
+    res = [cpu_baseline(wl, ks, budget_s=budget / 4, rows=16) for _ in range(args.steps)]
+    dt = time.time() - t0
+    value = statistics.median(r["value"] for r in res)
+    ms = dt / args.steps * 1e3
+    return {
+        "impl": "reference",
+        "metric": "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 GEMM of decoded MXFP8, f32 norm", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.m, "N": N_OUT, "K": list(ks), "norm_quant": f"{wl.m}x{H}",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res[0]["cores"], "kind": "oracle",
+                         "sample": res[0]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="m1024")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    out = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+"""Python binding of libmxgemm (MXFP8 Gemma-RMSNorm quantisation + block-scaled GEMM).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/mxgemm.h.  Functions named
+``mx_*`` mirror the C entry points one to one; they accept torch tensors
+(their device pointers are passed) or raw integer device addresses.  The
+small helpers at the bottom only allocate outputs with torch and call them.
+
+There is no fallback: if libmxgemm.so has not been built, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmxgemm.so")
+
+MX_STATUS = {
+    0: "MX_OK",
+    1: "MX_ERR_NULL",
+    2: "MX_ERR_ALIGN",
+    3: "MX_ERR_SHAPE",
+    4: "MX_ERR_ARCH",
+    5: "MX_ERR_CUDA",
+    6: "MX_ERR_DEVICE_TIMEOUT",
+}
+
+EXPORTED = (
+    "mx_scale_bytes", "mx_rmsnorm_quant", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+    "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
+)
+
+
+class MxError(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        self.status_name = MX_STATUS.get(status, str(status))
+        self.cuda_error = cuda_error
+        msg = f"{fn}: {self.status_name}"
+        if status == 5:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmxgemm.so (loaded on first use; raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libmxgemm.so is not built ({LIB_PATH} missing). Build it with "
+            "`python -m mxfp8_norm_quant_gb300.build` or `__graft_entry__.build()`; there is no fallback.")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, vp, u8p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+    L.mx_scale_bytes.argtypes = [i64, i64]
+    L.mx_scale_bytes.restype = ctypes.c_size_t
+    L.mx_rmsnorm_quant.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, vp]
+    L.mx_quant_weights.argtypes = [vp, u8p, u8p, i64, i64, vp]
+    L.mx_gemm.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, vp]
+    L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, vp]
+    L.mx_gemm_plan.argtypes = [i64, i64, i64, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
+    L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.mx_last_cuda_error.argtypes = []
+    L.mx_status_string.argtypes = [i32]
+    L.mx_status_string.restype = ctypes.c_char_p
+    L.mx_version.argtypes = []
+    for name in ("mx_rmsnorm_quant", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+                 "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream, *tensors) -> int | None:
+    if stream is None:
+        import torch
+        for t in tensors:
+            if hasattr(t, "is_cuda") and t.is_cuda:
+                return torch.cuda.current_stream(t.device).cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MxError(fn, status, lib().mx_last_cuda_error())
+
+
+# ------------------------------------------------------------- C entry points
+
+def mx_scale_bytes(rows: int, cols: int) -> int:
+    return int(lib().mx_scale_bytes(rows, cols))
+
+
+def mx_rmsnorm_quant(x, w, eps: float, out_q, out_scales, M: int, H: int, stream=None) -> None:
+    _check("mx_rmsnorm_quant", lib().mx_rmsnorm_quant(_ptr(x), _ptr(w), float(eps), _ptr(out_q), _ptr(out_scales),
+                                                      M, H, _stream(stream, x)))
+
+
+def mx_quant_weights(x, out_q, out_scales, rows: int, cols: int, stream=None) -> None:
+    _check("mx_quant_weights", lib().mx_quant_weights(_ptr(x), _ptr(out_q), _ptr(out_scales), rows, cols,
+                                                      _stream(stream, x)))
+
+
+def mx_gemm(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, stream=None) -> None:
+    _check("mx_gemm", lib().mx_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K,
+                                    _stream(stream, a_q)))
+
+
+def mx_gemm_ex(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, block_n: int, stream=None) -> None:
+    _check("mx_gemm_ex", lib().mx_gemm_ex(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K,
+                                          block_n, _stream(stream, a_q)))
+
+
+def mx_gemm_plan(M: int, N: int, K: int):
+    bn, st, gr = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check("mx_gemm_plan", lib().mx_gemm_plan(M, N, K, ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)))
+    return {"block_n": bn.value, "stages": st.value, "grid": gr.value}
+
+
+def mx_e4m3_encode_f32(inp, out, n: int, stream=None) -> None:
+    _check("mx_e4m3_encode_f32", lib().mx_e4m3_encode_f32(_ptr(inp), _ptr(out), n, _stream(stream, inp)))
+
+
+def mx_device_fault() -> int:
+    code = ctypes.c_uint32(0)
+    st = lib().mx_device_fault(ctypes.byref(code))
+    if st not in (0, 6):
+        _check("mx_device_fault", st)
+    return int(code.value)
+
+
+def mx_status_string(status: int) -> str:
+    return lib().mx_status_string(status).decode()
+
+
+def mx_version() -> int:
+    return int(lib().mx_version())
+
+
+# ------------------------------------------------------------- conveniences
+
+def rmsnorm_quant(x, w, eps: float = 1e-6, stream=None):
+    """Allocates (q, scales) for an (M, H) bf16 CUDA tensor and runs mx_rmsnorm_quant."""
+    import torch
+    M, H = x.shape
+    q = torch.empty((M, H), dtype=torch.uint8, device=x.device)
+    s = torch.empty(mx_scale_bytes(M, H), dtype=torch.uint8, device=x.device)
+    mx_rmsnorm_quant(x, w, eps, q, s, M, H, stream)
+    return q, s
+
+
+def quant(x, stream=None):
+    """Allocates (q, scales) for an (R, C) bf16 CUDA tensor and runs mx_quant_weights."""
+    import torch
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    s = torch.empty(mx_scale_bytes(R, C), dtype=torch.uint8, device=x.device)
+    mx_quant_weights(x, q, s, R, C, stream)
+    return q, s
+
+
+def gemm(a_q, a_s, b_q, b_s, block_n: int = 0, stream=None):
+    """C = A . B^T in bf16 for MXFP8 operands (A: M x K, B: N x K)."""
+    import torch
+    M, K = a_q.shape
+    N = b_q.shape[0]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, block_n, stream)
+    return out

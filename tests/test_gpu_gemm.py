@@ -1,0 +1,138 @@
+"""GPU parity of mx_gemm against the oracle's float64 GEMM of the decoded
+operands: exact special cases (which also pin the scale layout), random
+operands within |gpu - ref| <= 1e-2 (|ref| + 1) for every tile width and
+ragged shapes, and the full-size workloads on sampled rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import mxfp8_norm_quant_gb300 as mx
+import oracle as O
+from mxfp8_norm_quant_gb300 import workloads as W
+from mxtest import bf16_bits, gemm_close, np_u8, to_dev
+
+pytestmark = pytest.mark.gpu
+
+BLOCK_NS = [32, 64, 96, 128, 160, 192, 224]
+
+
+def _gemm(aq, as_, bq, bs, M, N, K, dev, block_n=0):
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    mx.mx_gemm_ex(to_dev(aq, dev), to_dev(as_, dev), to_dev(bq, dev), to_dev(bs, dev), out, M, N, K, block_n)
+    torch.cuda.synchronize()
+    assert mx.mx_device_fault() == 0
+    return out
+
+
+def _random_codes(rng, shape):
+    q = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x38                    # no NaN codes
+    return q
+
+
+@pytest.mark.parametrize("block_n", BLOCK_NS)
+def test_one_hot_b_selects_a_elements(cuda_dev, block_n):
+    # B row n = E4M3 1.0 at column k_n (scale byte 127): C[m, n] = dec(A)[m, k_n]
+    # exactly (4 significant bits fit bf16).  A's scale bytes vary by row and
+    # K-block, so a misplaced scale or row fails.
+    rng = np.random.default_rng(block_n)
+    M, N, K = 256, 448, 512
+    aq = _random_codes(rng, (M, K))
+    asb = rng.integers(110, 145, size=(M, K // 32), dtype=np.uint8)
+    kn = rng.integers(0, K, size=N)
+    bq = np.zeros((N, K), dtype=np.uint8)
+    bq[np.arange(N), kn] = 0x38
+    bsb = np.full((N, K // 32), 127, dtype=np.uint8)
+    ref = O.gemm_ref(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb))
+    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, block_n)
+    expect = torch.from_numpy(ref).float().to(torch.bfloat16)
+    assert torch.equal(got.cpu(), expect)
+
+
+@pytest.mark.parametrize("block_n", BLOCK_NS)
+def test_small_integers_exact(cuda_dev, block_n):
+    # entries in {-1, 0, 1} x power-of-two scales that differ per row and
+    # K-block of both operands: every partial sum is exact, so the bf16
+    # output is the RNE rounding of the exact result, bit for bit.
+    rng = np.random.default_rng(100 + block_n)
+    M, N, K = 384, 320, 640
+    ai = rng.integers(-1, 2, size=(M, K))
+    bi = rng.integers(-1, 2, size=(N, K))
+    aq = O.e4m3_encode(ai.astype(np.float32))
+    bq = O.e4m3_encode(bi.astype(np.float32))
+    # scales x1/x2 on A and x0.5/x1 on B: |partial sums| <= 1280 at a granularity
+    # of 0.5 (12 significant bits), exact even in a narrower accumulator
+    asb = rng.integers(127, 129, size=(M, K // 32), dtype=np.uint8)
+    bsb = rng.integers(126, 128, size=(N, K // 32), dtype=np.uint8)
+    ref = O.gemm_ref(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb))
+    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, block_n)
+    expect = torch.from_numpy(ref).float().to(torch.bfloat16)
+    assert torch.equal(got.cpu(), expect)
+
+
+SHAPES = [(128, 6144, 2048), (1, 96, 32), (300, 416, 288), (129, 256, 4096), (512, 1024, 3072), (77, 6144, 160),
+          (1000, 2016, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("block_n", [0] + BLOCK_NS)
+def test_random_within_tolerance(cuda_dev, M, N, K, block_n):
+    if block_n and M * N * K > 2 ** 31 and block_n not in (64, 192):
+        pytest.skip("large shape covered by the auto plan and two forced widths")
+    a, wt = W.gemm_operands(M, K, seed=M + N + K, n=N)
+    aq, as_ = O.quant(bf16_bits(a))
+    bq, bs_ = O.quant(bf16_bits(wt))
+    ref = O.gemm_ref(aq, as_, bq, bs_)
+    got = _gemm(aq, as_, bq, bs_, M, N, K, cuda_dev, block_n)
+    ok, worst = gemm_close(got, ref)
+    assert ok, f"worst err/tol = {worst:.3f}"
+
+
+def test_zero_m_is_noop(cuda_dev):
+    out = torch.full((4,), 3.0, dtype=torch.bfloat16, device=cuda_dev)
+    mx.mx_gemm(0, 0, 0, 0, out, 0, 6144, 2048)
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
+
+
+def _workload_check(wl, k, dev, n_rows=256, seed=0):
+    """The full-size GEMM exactly as bench.py launches it (operands quantised by
+    the GPU kernels, which are themselves checked bit-exact elsewhere), checked
+    on a row sample against the oracle."""
+    a, wt = wl.gemm(k, seed)
+    M, N = a.shape[0], wt.shape[0]
+    ad, wd = a.to(dev), wt.to(dev)
+    aq, as_ = mx.quant(ad)
+    bq, bs_ = mx.quant(wd)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    mx.mx_gemm(aq, as_, bq, bs_, out, M, N, k)
+    torch.cuda.synchronize()
+    assert mx.mx_device_fault() == 0
+    # operands for the oracle: from the oracle's own quantiser
+    rng = np.random.default_rng(seed + M + k)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, min(M, n_rows), replace=False)]))
+    bq_o, bs_o = O.quant(bf16_bits(wt))
+    aq_o, as_o = O.quant(bf16_bits(a[torch.from_numpy(rows)]))
+    ref = O.gemm_ref(aq_o, as_o, bq_o, bs_o)
+    ok, worst = gemm_close(out[torch.from_numpy(rows).to(dev)], ref)
+    assert ok, f"{wl.name} K={k}: worst err/tol = {worst:.3f}"
+    return worst
+
+
+@pytest.mark.parametrize("name,k", [("m128", 2048), ("m1024", 2048), ("m1024", 3072), ("m4096_rowscale", 2048),
+                                    ("m4096_rowscale", 3072), ("m32768_stress", 3072)])
+def test_workload_full_size_sampled(cuda_dev, name, k):
+    _workload_check(W.WORKLOADS[name], k, cuda_dev)
+
+
+@pytest.mark.parametrize("m", W.M_SWEEP)
+@pytest.mark.parametrize("k", [W.K_OPROJ, W.K_DOWN])
+def test_m_sweep_sampled(cuda_dev, m, k):
+    _workload_check(W.sweep_workload(m, k), k, cuda_dev, n_rows=96, seed=1)
+
+
+def test_plan_is_consistent(cuda_dev):
+    for m in W.M_SWEEP:
+        p = mx.mx_gemm_plan(m, 6144, 2048)
+        assert p["block_n"] in BLOCK_NS and p["stages"] >= 2 and p["grid"] >= 1
