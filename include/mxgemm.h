@@ -121,7 +121,7 @@ mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s,
                   void* out, int64_t M, int64_t N, int64_t K, mx_stream_t stream);
 
 /* mx_gemm with the tile width forced: block_n = 0 picks automatically,
- * otherwise one of 32, 64, 96, 128, 160, 192, 224 (MX_ERR_SHAPE otherwise). */
+ * otherwise one of 64, 128, 192 (MX_ERR_SHAPE otherwise). */
 mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s,
                      const uint8_t* b_q, const uint8_t* b_s,
                      void* out, int64_t M, int64_t N, int64_t K,

@@ -52,9 +52,9 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFA_BYTES = 512;
-  static constexpr int SFB_BYTES = 3 * 512;  // up to three 128-row scale blocks
+  static constexpr int SFB_BYTES = 2 * 512;  // up to two 128-row scale blocks
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SF_COLS = 16;  // TMEM columns per stage: 4 for A, 12 for B
+  static constexpr int SF_COLS = 12;  // TMEM columns per stage: 4 for A, 8 for B
   static constexpr int STAGES_SMEM = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES_TMEM = (TMEM_COLS - 2 * BN) / SF_COLS;
   static constexpr int STAGES_MIN = STAGES_SMEM < STAGES_TMEM ? STAGES_SMEM : STAGES_TMEM;
@@ -71,7 +71,7 @@ struct GemmCfg {
   static constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;  // + slack to align the base to 1 KB
   static constexpr int TMEM_SF = 2 * BN;
   static_assert(STAGES >= 2, "pipeline too shallow");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 192, "tile width");
   static_assert(B_BYTES % 1024 == 0, "B tiles keep the 1 KB swizzle-atom alignment");
 };
 
@@ -198,6 +198,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int n0 = nt * BN;
         const int nat = sfb_atoms(n0, BN, p.sfb_blocks);
         const uint32_t sfb_col = static_cast<uint32_t>((n0 & 127) >> 5);
+        if ((sfb_col & 1u) != 0 || nat > 2) {  // unreachable for BN % 64 == 0; never issue such an MMA
+          atomicOr(p.fault, FAULT_GEMM_MMA);
+          *abort_flag = 1;
+          break;
+        }
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, abort_flag)) {
           if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
@@ -360,19 +365,16 @@ int stages_of() {
 
 }  // namespace
 
-bool gemm_block_n_supported(int bn) {
-  return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 160 || bn == 192 || bn == 224;
-}
+// Tile widths are multiples of 64 so that a tile starts 0 or 64 rows into a
+// 128-row scale block: the B-scale TMEM address is then shifted by 0 or 2
+// columns (an odd column shift is not a valid scale address).
+bool gemm_block_n_supported(int bn) { return bn == 64 || bn == 128 || bn == 192; }
 
 int gemm_stages(int bn) {
   switch (bn) {
-    case 32: return stages_of<32>();
     case 64: return stages_of<64>();
-    case 96: return stages_of<96>();
     case 128: return stages_of<128>();
-    case 160: return stages_of<160>();
     case 192: return stages_of<192>();
-    case 224: return stages_of<224>();
     default: return 0;
   }
 }
@@ -382,7 +384,7 @@ int gemm_stages(int bn) {
 // waves of num_sms; a fixed per-tile overhead covers pipeline fill and the
 // last epilogue.
 int gemm_pick_block_n(int M, int N, int K, int num_sms) {
-  static const int cands[] = {64, 96, 128, 160, 192};
+  static const int cands[] = {64, 128, 192};
   const long long kt = (K + BK - 1) / BK;
   long long best = -1;
   int best_bn = 128;
@@ -407,13 +409,9 @@ int gemm_grid(int M, int N, int bn, int num_sms) {
 cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
                         int N, int K, int bn, int num_sms, unsigned int* fault, cudaStream_t stream) {
   switch (bn) {
-    case 32: return launch_bn<32>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
     case 64: return launch_bn<64>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 96: return launch_bn<96>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
     case 128: return launch_bn<128>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 160: return launch_bn<160>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
     case 192: return launch_bn<192>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 224: return launch_bn<224>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
     default: return cudaErrorInvalidValue;
   }
 }

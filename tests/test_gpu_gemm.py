@@ -14,7 +14,7 @@ from mxtest import bf16_bits, gemm_close, np_u8, to_dev
 
 pytestmark = pytest.mark.gpu
 
-BLOCK_NS = [32, 64, 96, 128, 160, 192, 224]
+BLOCK_NS = [64, 128, 192]
 
 
 def _gemm(aq, as_, bq, bs, M, N, K, dev, block_n=0):
@@ -78,8 +78,6 @@ SHAPES = [(128, 6144, 2048), (1, 96, 32), (300, 416, 288), (129, 256, 4096), (51
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("block_n", [0] + BLOCK_NS)
 def test_random_within_tolerance(cuda_dev, M, N, K, block_n):
-    if block_n and M * N * K > 2 ** 31 and block_n not in (64, 192):
-        pytest.skip("large shape covered by the auto plan and two forced widths")
     a, wt = W.gemm_operands(M, K, seed=M + N + K, n=N)
     aq, as_ = O.quant(bf16_bits(a))
     bq, bs_ = O.quant(bf16_bits(wt))
