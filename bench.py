@@ -146,7 +146,7 @@ def run_gpu(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     mx.lib()
-    wl = W.WORKLOADS[args.workload]
+    wl = W.get_workload(args.workload)
     M = wl.m
     ks = wl.ks
     stream = torch.cuda.Stream(dev)
@@ -183,8 +183,6 @@ def run_gpu(args, rank, world):
     wsets = [wq] + [{k: (wq[k][0].clone(), wq[k][1].clone()) for k in ks} for _ in range(R - 1)]
     torch.cuda.synchronize()
 
-    kernels = ["norm_quant"] + [f"quant_a{k}" for k in ks] + [f"gemm_k{k}" for k in ks]
-
     def step(i, ev=None):
         s = sets[i % R]
         wsx = wsets[i % R]
@@ -205,6 +203,18 @@ def run_gpu(args, rank, world):
             mx.mx_gemm(s[f"aq{k}"], s[f"as{k}"], wsx[k][0], wsx[k][1], s[f"c{k}"], M, N_OUT, k, sptr)
             mark()
 
+    def one_kernel(i, idx):
+        s = sets[i % R]
+        wsx = wsets[i % R]
+        if idx == 0:
+            mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], M, H, sptr)
+            return
+        k = ks[(idx - 1) // 2]
+        if (idx - 1) % 2 == 0:
+            mx.mx_quant_weights(s[f"a{k}"], s[f"aq{k}"], s[f"as{k}"], M, k, sptr)
+        else:
+            mx.mx_gemm(s[f"aq{k}"], s[f"as{k}"], wsx[k][0], wsx[k][1], s[f"c{k}"], M, N_OUT, k, sptr)
+
     n_marks = 2 + 2 * len(ks)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -212,41 +222,86 @@ def run_gpu(args, rank, world):
     stream.synchronize()
     assert mx.mx_device_fault() == 0
 
+    # The K timed steps are captured once as a CUDA graph (the launches go
+    # through the same C entry points; the graph removes the host's per-call
+    # launch latency, as a serving engine's CUDA-graph mode does).  A second
+    # graph of the same K steps carries timing events between the kernels for
+    # the per-kernel breakdown.
+    g_main = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_main, stream=stream):
+        for i in range(args.steps):
+            step(i)
+    in_graph_events = True
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_marks)]
+               for _ in range(args.steps)]
+        g_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ev, stream=stream):
+            for i in range(args.steps):
+                step(i, evs[i])
+    except TypeError:
+        in_graph_events = False
+    torch.cuda.synchronize()
+
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     # soak ~1.5 s so the clocks under load are sampled and settled
     t_soak = time.time()
-    i = 0
     with torch.cuda.stream(stream):
         while time.time() - t_soak < 1.5:
-            for _ in range(50):
-                step(i)
-                i += 1
+            for _ in range(5):
+                g_main.replay()
             stream.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(args.steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            step(i, evs[i])
+        e0.record(stream)
+        g_main.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t_wall1 = time.time()
-    sampler.stop()
-    assert mx.mx_device_fault() == 0
+    total_ms = e0.elapsed_time(e1)
 
-    total_ms = evs[0][0].elapsed_time(evs[-1][n_marks - 1])
-    per_kernel = {name: 0.0 for name in kernels}
+    # per-kernel durations over the same K steps (events inside the graph, or
+    # one graph of K back-to-back launches per kernel if events cannot be
+    # captured by this torch)
     order = ["norm_quant"]
     for k in ks:
         order += [f"quant_a{k}", f"gemm_k{k}"]
-    for e in evs:
-        for idx, name in enumerate(order):
-            per_kernel[name] += e[idx].elapsed_time(e[idx + 1])
+    per_kernel = {name: 0.0 for name in order}
+    with torch.cuda.stream(stream):
+        if in_graph_events:
+            g_ev.replay()
+            stream.synchronize()
+            for e in evs:
+                for idx, name in enumerate(order):
+                    per_kernel[name] += e[idx].elapsed_time(e[idx + 1])
+            breakdown_ms = evs[0][0].elapsed_time(evs[-1][n_marks - 1])
+        else:
+            breakdown_ms = 0.0
+            for idx, name in enumerate(order):
+                gk = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gk, stream=stream):
+                    for i in range(args.steps):
+                        one_kernel(i, idx)
+                b0 = torch.cuda.Event(enable_timing=True)
+                b1 = torch.cuda.Event(enable_timing=True)
+                b0.record(stream)
+                gk.replay()
+                b1.record(stream)
+                stream.synchronize()
+                per_kernel[name] = b0.elapsed_time(b1)
+                breakdown_ms += per_kernel[name]
+    torch.cuda.synchronize()
+    sampler.stop()
+    assert mx.mx_device_fault() == 0
     ms_per_step = total_ms / args.steps
 
     flops_step = sum(gemm_flops(M, N_OUT, k) for k in ks)
@@ -270,22 +325,23 @@ def run_gpu(args, rank, world):
     nq_ms = per_kernel["norm_quant"] / args.steps
     nq_gbs = norm_quant_bytes(M) / (nq_ms * 1e-3) / 1e9
     kern = {}
+    denom = breakdown_ms if breakdown_ms > 0 else total_ms
     for name in order:
         ms = per_kernel[name] / args.steps
         if name == "norm_quant":
             b = norm_quant_bytes(M)
             kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
-                          peaks["hbm_gbs"], "share": per_kernel[name] / total_ms}
+                          peaks["hbm_gbs"], "share": per_kernel[name] / denom}
         elif name.startswith("quant_a"):
             k = int(name[7:])
             b = quant_bytes(M, k)
             kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
-                          peaks["hbm_gbs"], "share": per_kernel[name] / total_ms}
+                          peaks["hbm_gbs"], "share": per_kernel[name] / denom}
         else:
             k = int(name[6:])
             f = gemm_flops(M, N_OUT, k)
             kern[name] = {"us": ms * 1e3, "TFLOP/s": f / (ms * 1e-3) / 1e12,
-                          "frac_fp8": f / (ms * 1e-3) / 1e12 / fp8_peak, "share": per_kernel[name] / total_ms}
+                          "frac_fp8": f / (ms * 1e-3) / 1e12 / fp8_peak, "share": per_kernel[name] / denom}
     plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
 
     clocks = sampler.summary(t_soak, t_wall1)
@@ -319,6 +375,9 @@ def run_gpu(args, rank, world):
                                 "frac": nq_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
         "e2e": e2e,
         "gpu_launches": len(order) * args.steps,
+        "timing": {"timed_region": "one CUDA-graph replay of the K steps (CUDA events on the launch stream)",
+                   "per_kernel": "timing events inside a second graph of the same K steps" if in_graph_events
+                   else "one graph of K back-to-back launches per kernel"},
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
@@ -388,11 +447,8 @@ def _oracle_threads():
     return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, ks, budget_s=15.0, rows=16):
-    """The oracle as it stands, on a bounded row sample of one step: norm-quant of
-    `rows` rows of x, quantisation of `rows` rows of each A, and their GEMM rows
-    against the full weight (quantised and decoded by the oracle).  Repeated
-    until budget_s of CPU time; scaled to TFLOP/s of GEMM work."""
+def _oracle_prepare(wl, ks, rows):
+    """Untimed: seeded inputs as the oracle takes them, weights quantised by the oracle."""
     import numpy as np
     import torch
 
@@ -402,55 +458,149 @@ def cpu_baseline(wl, ks, budget_s=15.0, rows=16):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
     x, w = wl.norm(seed=0)
-    xs = bits(x[:rows])
-    wb = bits(w)
     ops = []
     for k in ks:
         a, wt = wl.gemm(k, seed=0)
         bq, bs = O.quant(bits(wt))
         ops.append((k, bits(a[:rows]), bq, bs))
+    return {"x": bits(x[:rows]), "w": bits(w), "ops": ops, "rows": rows}
+
+
+def _oracle_step(prep):
+    """One bounded sample of a step, run by the oracle as it stands: norm-quant
+    of `rows` rows of x, quantisation of `rows` rows of each A, and their GEMM
+    rows against the full 6144-row weight.  Returns the GEMM flops done."""
+    import oracle as O
+    O.rmsnorm_quant(prep["x"], prep["w"], EPS)
     flops = 0.0
-    t0 = time.time()
+    for k, ab, bq, bs in prep["ops"]:
+        aq, as_ = O.quant(ab)
+        O.gemm_ref(aq, as_, bq, bs)
+        flops += gemm_flops(prep["rows"], N_OUT, k)
+    return flops
+
+
+def _sample_text(wl, ks, rows, n, dt):
+    return (f"{n} x ({rows} rows of norm-quant {wl.m}x{H}; {rows} rows of quant + GEMM vs the full "
+            f"6144-row weight for K={list(ks)}), {dt:.1f} s")
+
+
+def cpu_baseline(wl, ks, budget_s=15.0, rows=16):
+    """The oracle timed on a bounded row sample of the step, repeated for about
+    budget_s seconds; reported as TFLOP/s of GEMM work."""
+    prep = _oracle_prepare(wl, ks, rows)
+    flops = 0.0
     n = 0
+    t0 = time.time()
     while True:
-        O.rmsnorm_quant(xs, wb, EPS)
-        for k, ab, bq, bs in ops:
-            aq, as_ = O.quant(ab)
-            O.gemm_ref(aq, as_, bq, bs)
-            flops += gemm_flops(rows, N_OUT, k)
+        flops += _oracle_step(prep)
         n += 1
         if time.time() - t0 >= budget_s:
             break
     dt = time.time() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
-            "sample": f"{n} x ({rows} rows of norm-quant {wl.m}x{H}; {rows} rows of quant + GEMM vs the full "
-                      f"6144-row weight for K={list(ks)}), {dt:.1f} s"}
+            "sample": _sample_text(wl, ks, rows, n, dt)}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, each step one bounded sample of the workload."""
     from mxfp8_norm_quant_gb300 import workloads as W
-    wl = W.WORKLOADS[args.workload]
+    wl = W.get_workload(args.workload)
     ks = wl.ks
-    budget = max(2.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    rows = 16
+    prep = _oracle_prepare(wl, ks, rows)
     for _ in range(args.warmup):
-        cpu_baseline(wl, ks, budget_s=0.0, rows=8)
+        _oracle_step(prep)
     t0 = time.time()
-    res = [cpu_baseline(wl, ks, budget_s=budget / 4, rows=16) for _ in range(args.steps)]
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += _oracle_step(prep)
     dt = time.time() - t0
-    value = statistics.median(r["value"] for r in res)
-    ms = dt / args.steps * 1e3
+    value = flops / dt / 1e12
     return {
         "impl": "reference",
         "metric": "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 GEMM of decoded MXFP8, f32 norm", "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.m, "N": N_OUT, "K": list(ks), "norm_quant": f"{wl.m}x{H}",
                    "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res[0]["cores"], "kind": "oracle",
-                         "sample": res[0]["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
+                         "sample": _sample_text(wl, ks, rows, args.steps, dt)},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def run_one_kernel(args):
+    """--kernel mode: one kernel of the path, launched eagerly `steps` times on
+    rotating buffers after `warmup` launches (used for ncu captures and sweeps).
+    Reports the mean device time per launch from CUDA events."""
+    import torch
+
+    import mxfp8_norm_quant_gb300 as mx
+    from mxfp8_norm_quant_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.get_workload(args.workload)
+    M = wl.m
+    k = args.k if args.k else wl.ks[-1]
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    R = 3
+    if args.kernel == "norm_quant":
+        x, w = wl.norm()
+        xs = [x.to(dev) for _ in range(R)]
+        wd = w.to(dev)
+        qs = [torch.empty((M, H), dtype=torch.uint8, device=dev) for _ in range(R)]
+        ss = [torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+        def launch(i):
+            mx.mx_rmsnorm_quant(xs[i % R], wd, EPS, qs[i % R], ss[i % R], M, H, sptr)
+        work, unit = norm_quant_bytes(M) / 1e9, "GB/s"
+    elif args.kernel == "quant":
+        a, _ = wl.gemm(k)
+        xs = [a.to(dev) for _ in range(R)]
+        qs = [torch.empty((M, k), dtype=torch.uint8, device=dev) for _ in range(R)]
+        ss = [torch.empty(mx.mx_scale_bytes(M, k), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+        def launch(i):
+            mx.mx_quant_weights(xs[i % R], qs[i % R], ss[i % R], M, k, sptr)
+        work, unit = quant_bytes(M, k) / 1e9, "GB/s"
+    elif args.kernel == "gemm":
+        a, wt = wl.gemm(k)
+        ops = [mx.quant(a.to(dev)) for _ in range(R)]
+        wqs = [mx.quant(wt.to(dev)) for _ in range(R)]
+        outs = [torch.empty((M, N_OUT), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+        def launch(i):
+            j = i % R
+            mx.mx_gemm_ex(ops[j][0], ops[j][1], wqs[j][0], wqs[j][1], outs[j], M, N_OUT, k, args.block_n, sptr)
+        work, unit = gemm_flops(M, N_OUT, k) / 1e12, "TFLOP/s"
+    else:
+        raise SystemExit(f"unknown --kernel {args.kernel}")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(i)
+        stream.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            launch(i)
+            evs[i][1].record(stream)
+        stream.synchronize()
+    assert mx.mx_device_fault() == 0
+    ms = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(ms)
+    out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel != "norm_quant" else None,
+           "launches": args.steps, "us_median": med * 1e3, "us_min": min(ms) * 1e3,
+           "rate_median": work / (med * 1e-3), "rate_best": work / (min(ms) * 1e-3), "unit": unit}
+    if args.kernel == "gemm":
+        out["plan"] = mx.mx_gemm_plan(M, N_OUT, k)
+        out["block_n"] = args.block_n or out["plan"]["block_n"]
+    print(json.dumps(out), flush=True)
 
 
 def main():
@@ -462,12 +612,19 @@ def main():
     ap.add_argument("--workload", default="m1024")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["norm_quant", "quant", "gemm"],
+                    help="time one kernel of the path alone (eager launches)")
+    ap.add_argument("--k", type=int, default=0, help="--kernel mode: contraction size (default: workload's last)")
+    ap.add_argument("--block-n", type=int, default=0, help="--kernel gemm: force the tile width")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.kernel:
+        run_one_kernel(args)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world)), flush=True)

@@ -80,6 +80,35 @@ mx_status check_gemm(int64_t M, int64_t N, int64_t K) {
 
 }  // namespace
 
+namespace mxk {
+
+cudaError_t set_smem_once(const void* kernel, int bytes) {
+  struct Entry {
+    const void* fn;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Entry table[256];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].fn == kernel && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) table[i].bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && used < 256) table[used++] = Entry{kernel, dev, bytes};
+  return e;
+}
+
+}  // namespace mxk
+
 MX_API size_t mx_scale_bytes(int64_t rows, int64_t cols) {
   if (rows < 0 || cols < 0 || cols % 32 != 0) return 0;
   const int64_t c = cols / 32;

@@ -350,7 +350,7 @@ cudaError_t launch_bn(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, c
   p.sfb_blocks = (N + 127) / 128;
   p.fault = fault;
   auto kern = k_gemm_mxf8<BN>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  err = set_smem_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = tiles < num_sms ? tiles : num_sms;

@@ -265,7 +265,7 @@ cudaError_t launch_row(const uint16_t* x, const uint16_t* w, float eps, uint8_t*
   if (stages < 2) stages = 2;
   const SmemLayout L = row_smem_layout(H, stages, Cfg::GROUPS);
   auto kern = k_row_quant<NORM, CPW>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), L.total);
   if (err != cudaSuccess) return err;
   const int Mp = ((M + 127) / 128) * 128;
   int grid = num_sms;

@@ -7,6 +7,10 @@
 
 namespace mxk {
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the CUDA call is made only when the limit grows.
+cudaError_t set_smem_once(const void* kernel, int bytes);
+
 cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                                  int num_sms, unsigned int* fault, cudaStream_t stream);
 cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,

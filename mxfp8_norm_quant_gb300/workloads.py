@@ -138,4 +138,14 @@ WORKLOADS = {
 
 
 def sweep_workload(m: int, k: int) -> Workload:
-    return Workload(f"sweep_m{m}_k{k}", m, (k,), 0, notes="M sweep, plain N(0,1) activations")
+    return Workload(f"sweep_m{m}_k{k}", m, (k,), m, notes="M sweep, plain N(0,1) activations")
+
+
+def get_workload(name: str) -> Workload:
+    """A named workload, or sweep_m<M>_k<K> for a point of the M x K sweep."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name.startswith("sweep_m") and "_k" in name:
+        m, k = name[len("sweep_m"):].split("_k")
+        return sweep_workload(int(m), int(k))
+    raise KeyError(f"unknown workload {name!r}; known: {sorted(WORKLOADS)} or sweep_m<M>_k<K>")
