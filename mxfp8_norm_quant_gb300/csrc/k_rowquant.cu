@@ -6,20 +6,25 @@
 // with the scales in the F8_128x4 layout the GEMM consumes (PR #64659,
 // Details / "GEMM-RS with a quantized input").
 //
-// Design (HBM-bound, ~3 bytes moved per element):
-//   * persistent grid, one CTA per SM; warp 0 is a TMA producer that streams
-//     whole rows (2*H bytes each) into a ring of shared-memory stages with
-//     cp.async.bulk, so ~150 KB per SM is in flight;
-//   * GROUPS groups of 8 consumer warps; a group owns one row at a time,
-//     lane l of warp v handles the 8 elements [256*c + 8*l, +8) of each
-//     256-element chunk c = v, v+8, ...;
-//   * the sum of squares follows the pairwise tree exactly: an 8-leaf tree
-//     inside the lane, a xor-butterfly over the 32 lanes (masks 1..16, i.e.
-//     the next five tree levels of the chunk), then a tree over the chunk
-//     sums (zero-padded to a power of two);
+// Both kernels are HBM-bound (about 3 bytes per element: 2 read, 1 written)
+// and are built to spend few instructions per element and keep many bytes in
+// flight:
+//   * a row is owned by WPR warps (1, 2 or 4); each lane owns 8 consecutive
+//     elements of every 256-element chunk it holds (one 16-byte load per
+//     chunk), and the whole row is loaded into registers with back-to-back
+//     16-byte loads before any arithmetic;
+//   * fp32 arithmetic uses the packed f32x2 instructions (two independent
+//     correctly rounded operations each);
+//   * the sum of squares is the pairwise tree exactly: the 8 leaves of a
+//     lane, then a xor-butterfly over the 32 lanes (masks 1..16 are the next
+//     five tree levels of the chunk), then the tree over the chunks, built
+//     incrementally as a binary counter and closed with zero subtrees; with
+//     WPR > 1 every warp owns an aligned power-of-two run of chunks and the
+//     warp subtotals are added in tree order through shared memory;
 //   * 4 lanes hold one 32-element MX block: amax by two shuffles, the UE8M0
 //     byte from the exponent field, one cvt per element pair, an 8-byte
 //     store of codes per lane and one 4-byte store per 4 scales.
+// No kernel here waits on a barrier other than bar.sync / __syncthreads.
 #include <cstdint>
 
 #include "mx_kernels.h"
@@ -29,29 +34,15 @@ namespace mxk {
 
 namespace {
 
-constexpr int CWARPS = 8;  // consumer warps per group
+constexpr int ROW_WARPS = 16;
+constexpr int ROW_THREADS = ROW_WARPS * 32;
 
-template <int CPW>
-struct RowCfg {
-  static constexpr int GROUPS = CPW <= 4 ? 2 : 1;
-  static constexpr int THREADS = 32 + GROUPS * CWARPS * 32;
-  static constexpr int MAXCHUNK = 8 * CPW;
-  static constexpr int TREE = MAXCHUNK <= 8 ? 8 : MAXCHUNK <= 16 ? 16 : MAXCHUNK <= 32 ? 32 : 64;
-};
-
-struct SmemLayout {
-  int stage_bytes, stages, red_off, bar_off, abort_off, total;
-};
-
-__host__ __device__ inline SmemLayout row_smem_layout(int H, int stages, int groups) {
-  SmemLayout L;
-  L.stage_bytes = ((H + 255) / 256) * 512;
-  L.stages = stages;
-  L.red_off = stages * L.stage_bytes;
-  L.bar_off = L.red_off + groups * 2 * 64 * 4;
-  L.abort_off = L.bar_off + (2 * stages + groups) * 8;
-  L.total = L.abort_off + 16;
-  return L;
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
 }
 
 // byte offset of the 4-scale word (r, 4*wd) in the F8_128x4 layout
@@ -59,250 +50,247 @@ __device__ __forceinline__ size_t scale_word_off(int r, int wd, int words) {
   return (static_cast<size_t>(r >> 7) * words + wd) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-__device__ __forceinline__ float tree8_squares(const uint4& v) {
-  const float x0 = bf16lo(v.x), x1 = bf16hi(v.x), x2 = bf16lo(v.y), x3 = bf16hi(v.y);
-  const float x4 = bf16lo(v.z), x5 = bf16hi(v.z), x6 = bf16lo(v.w), x7 = bf16hi(v.w);
-  const float a = __fadd_rn(__fmul_rn(x0, x0), __fmul_rn(x1, x1));
-  const float b = __fadd_rn(__fmul_rn(x2, x2), __fmul_rn(x3, x3));
-  const float c = __fadd_rn(__fmul_rn(x4, x4), __fmul_rn(x5, x5));
-  const float d = __fadd_rn(__fmul_rn(x6, x6), __fmul_rn(x7, x7));
-  return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+// Pairwise tree of the 8 squares held by one lane:
+// ((e0+e1)+(e2+e3)) + ((e4+e5)+(e6+e7)); the packed pairs (x0,x4), (x1,x5),
+// (x2,x6), (x3,x7) make each packed add one level of the tree.
+__device__ __forceinline__ float lane_square_tree(const uint4& v) {
+  const float2 a = make_float2(bf16lo(v.x), bf16lo(v.z));
+  const float2 b = make_float2(bf16hi(v.x), bf16hi(v.z));
+  const float2 c = make_float2(bf16lo(v.y), bf16lo(v.w));
+  const float2 d = make_float2(bf16hi(v.y), bf16hi(v.w));
+  const float2 l1a = __fadd2_rn(__fmul2_rn(a, a), __fmul2_rn(b, b));  // (e0+e1, e4+e5)
+  const float2 l1b = __fadd2_rn(__fmul2_rn(c, c), __fmul2_rn(d, d));  // (e2+e3, e6+e7)
+  const float2 l2 = __fadd2_rn(l1a, l1b);
+  return __fadd_rn(l2.x, l2.y);
 }
 
-template <bool NORM, int CPW>
-__global__ void __launch_bounds__(RowCfg<CPW>::THREADS, 1)
-    k_row_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
-                uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, int stages,
-                unsigned int* fault) {
-  using Cfg = RowCfg<CPW>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout L = row_smem_layout(H, stages, Cfg::GROUPS);
+// Tree over the 32 lanes of a warp (lane l holds leaf l); result in all lanes.
+__device__ __forceinline__ float warp_tree(float p) {
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, m));
+  return p;
+}
+
+// Quantises the 8 values a lane holds (4 lanes = one MX block) and stores
+// their codes and, from lanes 0 and 16, the two 4-scale words of the
+// 256-element chunk c of row `row`.
+__device__ __forceinline__ void quantize_store(float2 y01, float2 y23, float2 y45, float2 y67, bool valid,
+                                               int lane, int row, int c, int H, int words, uint8_t* __restrict__ q,
+                                               uint8_t* __restrict__ sc) {
+  float amax = fmaxf(fmaxf(fmaxf(fabsf(y01.x), fabsf(y01.y)), fmaxf(fabsf(y23.x), fabsf(y23.y))),
+                     fmaxf(fmaxf(fabsf(y45.x), fabsf(y45.y)), fmaxf(fabsf(y67.x), fabsf(y67.y))));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const uint32_t byte = ue8m0_from_amax(amax);
+  const float inv = inv_scale_from_ue8m0(byte);
+  const float2 iv = make_float2(inv, inv);
+  const float2 t01 = __fmul2_rn(y01, iv), t23 = __fmul2_rn(y23, iv);
+  const float2 t45 = __fmul2_rn(y45, iv), t67 = __fmul2_rn(y67, iv);
+  uint2 codes;
+  codes.x = cvt_e4m3x2(t01.x, t01.y) | (cvt_e4m3x2(t23.x, t23.y) << 16);
+  codes.y = cvt_e4m3x2(t45.x, t45.y) | (cvt_e4m3x2(t67.x, t67.y) << 16);
+  const int col = c * 256 + lane * 8;
+  if (valid) *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * H + col) = codes;
+  // the four scale bytes of each 128-element word: block b = lane / 4
+  uint32_t wv = valid ? byte << (8 * ((lane >> 2) & 3)) : 0u;
+  wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+  wv |= __shfl_xor_sync(0xffffffffu, wv, 8);
+  const int wd = 2 * c + (lane >> 4);
+  if ((lane & 15) == 0 && wd < words) *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = wv;
+}
+
+// --------------------------------------------------------------- fused norm
+
+// WPR warps per row, NCH chunks of 256 elements per warp (a power of two when
+// WPR > 1, so that every warp's chunks form an aligned subtree).
+template <int WPR, int NCH>
+__global__ void __launch_bounds__(ROW_THREADS, 1)
+    k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
+                    uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H) {
+  static_assert(WPR == 1 || (NCH & (NCH - 1)) == 0, "multi-warp rows need power-of-two chunk runs");
+  constexpr int GROUPS = ROW_WARPS / WPR;
+  extern __shared__ float g_s[];  // (1 + w) in fp32, zero-padded to whole chunks
+  __shared__ float red[GROUPS][2][4];
+
   const int nchunk = (H + 255) >> 8;
-  const int words = (H / 32 + 3) / 4;  // 4-scale words per row (Cp / 4)
+  const int words = (H / 32 + 3) / 4;
   const int Mp = ((M + 127) / 128) * 128;
-  float* red = reinterpret_cast<float*>(smem + L.red_off);
-  const uint32_t bar_full = smem_u32(smem + L.bar_off);
-  const uint32_t bar_empty = bar_full + 8 * stages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_off);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / WPR, wi = warp % WPR;
+  const int c0 = wi * NCH;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, CWARPS);
-    }
-    for (int gi = 0; gi < Cfg::GROUPS; ++gi) mbar_init(bar_full + 8 * (2 * stages + gi), CWARPS);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
+  for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
+    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
   __syncthreads();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
-      uint32_t it = 0;
-      for (int row = blockIdx.x; row < Mp; row += gridDim.x, ++it) {
-        const uint32_t s = it % stages, ph = (it / stages) & 1u;
-        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
-          if (*abort_flag == 0) atomicOr(fault, FAULT_ROWQ_PRODUCER);
-          *abort_flag = 1;
-          break;
-        }
-        if (row < M) {
-          mbar_arrive_expect_tx(bar_full + 8 * s, row_bytes);
-          bulk_g2s(smem_u32(smem + s * L.stage_bytes), x + static_cast<size_t>(row) * H, row_bytes,
-                   bar_full + 8 * s);
-        } else {
-          mbar_arrive(bar_full + 8 * s);  // padding row: no data, scales only
-        }
-      }
-      // Let every issued copy land before the CTA can exit (normally a no-op).
-      const uint32_t issued = it;
-      for (uint32_t s = 0; s < static_cast<uint32_t>(stages) && s < issued; ++s) {
-        const uint32_t last = s + ((issued - 1 - s) / stages) * stages;
-        if (!mbar_wait(bar_full + 8 * s, (last / stages) & 1u, nullptr, DRAIN_LIMIT_NS))
-          atomicOr(fault, FAULT_DRAIN);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int gidx = (warp - 1) / CWARPS;
-    const int v = (warp - 1) % CWARPS;
-
-    float g[NORM ? CPW : 1][8];
-    if constexpr (NORM) {
-#pragma unroll
-      for (int j = 0; j < CPW; ++j) {
-        const int col = (v + 8 * j) * 256 + lane * 8;
-        uint4 wv = make_uint4(0, 0, 0, 0);
-        if (col < H) wv = *reinterpret_cast<const uint4*>(w + col);
-        g[j][0] = __fadd_rn(1.0f, bf16lo(wv.x));
-        g[j][1] = __fadd_rn(1.0f, bf16hi(wv.x));
-        g[j][2] = __fadd_rn(1.0f, bf16lo(wv.y));
-        g[j][3] = __fadd_rn(1.0f, bf16hi(wv.y));
-        g[j][4] = __fadd_rn(1.0f, bf16lo(wv.z));
-        g[j][5] = __fadd_rn(1.0f, bf16hi(wv.z));
-        g[j][6] = __fadd_rn(1.0f, bf16lo(wv.w));
-        g[j][7] = __fadd_rn(1.0f, bf16hi(wv.w));
-      }
-    }
-
-    // group barrier: the group's 8 warps publish their chunk sums, then all
-    // read them (an mbarrier rather than bar.sync, so that waiting on it is
-    // bounded too)
-    const uint32_t bar_group = bar_full + 8 * (2 * stages + gidx);
-    uint32_t k = 0, nreal = 0;
-    for (int row = blockIdx.x + gidx * gridDim.x, it = gidx; row < Mp;
-         row += Cfg::GROUPS * gridDim.x, it += Cfg::GROUPS, ++k) {
-      const uint32_t s = it % stages, ph = (it / stages) & 1u;
-      if (!warp_wait(bar_full + 8 * s, ph, abort_flag)) {
-        if (lane == 0) {
-          if (*abort_flag == 0) atomicOr(fault, FAULT_ROWQ_CONSUMER);
-          *abort_flag = 1;
-        }
-        break;
-      }
-      if (row >= M) {
-        // padding row of the last 128-row block: its scale bytes are zero
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        for (int wd = v * 32 + lane; wd < words; wd += CWARPS * 32)
+  int it = 0;
+  for (int row = blockIdx.x + gridDim.x * grp; row < Mp; row += gridDim.x * GROUPS, ++it) {
+    if (row >= M) {
+      // padding row of the last 128-row block: its scale bytes are zero
+      if (wi == 0)
+        for (int wd = lane; wd < words; wd += 32)
           *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
-        continue;
-      }
+      continue;
+    }
+    const uint16_t* xr = x + static_cast<size_t>(row) * H;
+    uint4 xv[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int col = (c0 + j) * 256 + lane * 8;
+      xv[j] = col < H ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
+    }
 
-      const uint8_t* stg = smem + s * L.stage_bytes;
-      uint4 xv[CPW];
+    // pass 1: sum of squares, pairwise tree over the warp's chunks
+    float lvl[6];
 #pragma unroll
-      for (int j = 0; j < CPW; ++j) {
-        const int c = v + 8 * j;
-        xv[j] = make_uint4(0, 0, 0, 0);
-        if (c < nchunk && c * 256 + lane * 8 < H) xv[j] = *reinterpret_cast<const uint4*>(stg + c * 512 + lane * 16);
+    for (int j = 0; j < NCH; ++j) {
+      float t = warp_tree(lane_square_tree(xv[j]));
+      int k = 0;
+#pragma unroll
+      for (; k < 6; ++k) {
+        if (((j >> k) & 1) == 0) break;
+        t = __fadd_rn(lvl[k], t);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // this warp is done with the stage
-
-      float r = 1.0f;
-      if constexpr (NORM) {
-        float* red_row = red + (gidx * 2 + (k & 1)) * 64;
+      lvl[k] = t;
+    }
+    // close the tree with zero subtrees: fold the pending subtrees, smallest first
+    float ss_w = 0.0f;
+    bool first = true;
 #pragma unroll
-        for (int j = 0; j < CPW; ++j) {
-          float p = tree8_squares(xv[j]);
-#pragma unroll
-          for (int m = 1; m < 32; m <<= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, m));
-          const int c = v + 8 * j;
-          if (lane == 0 && c < nchunk) red_row[c] = p;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_group);
-        if (!warp_wait(bar_group, nreal & 1u, abort_flag)) {
-          if (lane == 0) {
-            if (*abort_flag == 0) atomicOr(fault, FAULT_ROWQ_CONSUMER);
-            *abort_flag = 1;
-          }
-          break;
-        }
-        ++nreal;
-        float t[Cfg::TREE];
-#pragma unroll
-        for (int i = 0; i < Cfg::TREE; ++i) t[i] = i < nchunk ? red_row[i] : 0.0f;
-#pragma unroll
-        for (int width = Cfg::TREE / 2; width >= 1; width >>= 1) {
-#pragma unroll
-          for (int i = 0; i < width; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
-        }
-        const float ms = __fdiv_rn(t[0], static_cast<float>(H));
-        r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-      }
-
-#pragma unroll
-      for (int j = 0; j < CPW; ++j) {
-        const int c = v + 8 * j;
-        if (c >= nchunk) continue;  // warp-uniform
-        const int col = c * 256 + lane * 8;
-        const bool valid = col < H;
-        float y[8] = {bf16lo(xv[j].x), bf16hi(xv[j].x), bf16lo(xv[j].y), bf16hi(xv[j].y),
-                      bf16lo(xv[j].z), bf16hi(xv[j].z), bf16lo(xv[j].w), bf16hi(xv[j].w)};
-        if constexpr (NORM) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(y[e], r), g[j][e]);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[e]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const uint32_t byte = ue8m0_from_amax(amax);
-        const float inv = inv_scale_from_ue8m0(byte);
-        uint2 codes;
-        codes.x = cvt_e4m3x2(__fmul_rn(y[0], inv), __fmul_rn(y[1], inv)) |
-                  (cvt_e4m3x2(__fmul_rn(y[2], inv), __fmul_rn(y[3], inv)) << 16);
-        codes.y = cvt_e4m3x2(__fmul_rn(y[4], inv), __fmul_rn(y[5], inv)) |
-                  (cvt_e4m3x2(__fmul_rn(y[6], inv), __fmul_rn(y[7], inv)) << 16);
-        if (valid) *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * H + col) = codes;
-        // gather the four scale bytes of each 128-element word: block b = lane/4
-        uint32_t wv = valid ? byte << (8 * ((lane >> 2) & 3)) : 0u;
-        wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
-        wv |= __shfl_xor_sync(0xffffffffu, wv, 8);
-        const int wd = 2 * c + (lane >> 4);
-        if ((lane & 15) == 0 && wd < words)
-          *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = wv;
+    for (int k = 0; k < 6; ++k) {
+      if ((NCH >> k) & 1) {
+        ss_w = first ? lvl[k] : __fadd_rn(lvl[k], ss_w);
+        first = false;
       }
     }
+    float ss = ss_w;
+    if constexpr (WPR > 1) {
+      if (lane == 0) red[grp][it & 1][wi] = ss_w;
+      named_barrier_sync(1 + grp, WPR * 32);
+      const float* rr = red[grp][it & 1];
+      if constexpr (WPR == 2) {
+        ss = __fadd_rn(rr[0], rr[1]);
+      } else {
+        ss = __fadd_rn(__fadd_rn(rr[0], rr[1]), __fadd_rn(rr[2], rr[3]));
+      }
+    }
+    // the packed row stays live across the reduction; re-unpacking it in
+    // pass 2 is cheaper than keeping every unpacked float alive
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) asm volatile("" : "+r"(xv[j].x), "+r"(xv[j].y), "+r"(xv[j].z), "+r"(xv[j].w));
+    const float ms = __fdiv_rn(ss, static_cast<float>(H));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    const float2 rr2 = make_float2(r, r);
+
+    // pass 2: y = (x * r) * (1 + w), then MX quantisation
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = c0 + j;
+      if (c >= nchunk) break;  // warp-uniform
+      const int col = c * 256 + lane * 8;
+      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
+      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
+      const uint4 v = xv[j];
+      const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
+      const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
+      const float2 y45 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr2), make_float2(gb.x, gb.y));
+      const float2 y67 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr2), make_float2(gb.z, gb.w));
+      quantize_store(y01, y23, y45, y67, col < H, lane, row, c, H, words, q, sc);
+      // keep the next chunk's shared-memory loads from being hoisted above
+      // this point (hoisting them all costs more registers than it hides)
+      asm volatile("" ::: "memory");
+    }
   }
-  __syncthreads();
 }
 
-template <bool NORM, int CPW>
-cudaError_t launch_row(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                       int num_sms, unsigned int* fault, cudaStream_t stream) {
-  using Cfg = RowCfg<CPW>;
-  const int stage_bytes = ((H + 255) / 256) * 512;
-  int stages = (160 * 1024) / stage_bytes;
-  if (stages > 16) stages = 16;
-  if (stages < 2) stages = 2;
-  const SmemLayout L = row_smem_layout(H, stages, Cfg::GROUPS);
-  auto kern = k_row_quant<NORM, CPW>;
-  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), L.total);
+// --------------------------------------------------------------- plain quant
+
+// A warp task is up to G consecutive chunks of one row.
+template <int G>
+__global__ void __launch_bounds__(ROW_THREADS, 2)
+    k_quant(const uint16_t* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int rows,
+            int cols) {
+  const int nchunk = (cols + 255) >> 8;
+  const int words = (cols / 32 + 3) / 4;
+  const int Mp = ((rows + 127) / 128) * 128;
+  const int tpr = (nchunk + G - 1) / G;
+  const long long ntask = static_cast<long long>(rows) * tpr;
+  const long long nall = ntask + (Mp - rows);
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * ROW_WARPS;
+  for (long long task = static_cast<long long>(blockIdx.x) * ROW_WARPS + (threadIdx.x >> 5); task < nall;
+       task += nwarps) {
+    if (task >= ntask) {
+      const int row = rows + static_cast<int>(task - ntask);
+      for (int wd = lane; wd < words; wd += 32)
+        *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
+      continue;
+    }
+    const int row = static_cast<int>(task / tpr);
+    const int c0 = static_cast<int>(task % tpr) * G;
+    const uint16_t* xr = x + static_cast<size_t>(row) * cols;
+    uint4 xv[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int col = (c0 + j) * 256 + lane * 8;
+      xv[j] = col < cols ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int c = c0 + j;
+      if (c >= nchunk) break;  // warp-uniform
+      const uint4 v = xv[j];
+      quantize_store(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
+                     make_float2(bf16lo(v.z), bf16hi(v.z)), make_float2(bf16lo(v.w), bf16hi(v.w)),
+                     c * 256 + lane * 8 < cols, lane, row, c, cols, words, q, sc);
+    }
+  }
+}
+
+template <int WPR, int NCH>
+cudaError_t launch_norm(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
+                        int num_sms, cudaStream_t stream) {
+  auto kern = k_rmsnorm_quant<WPR, NCH>;
+  const int smem = ((H + 255) / 256) * 256 * 4;
+  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const int Mp = ((M + 127) / 128) * 128;
-  int grid = num_sms;
-  if (grid > Mp) grid = Mp;
-  kern<<<grid, Cfg::THREADS, L.total, stream>>>(x, w, eps, q, sc, M, H, stages, fault);
+  const int grid = Mp < num_sms ? Mp : num_sms;
+  kern<<<grid, ROW_THREADS, smem, stream>>>(x, w, eps, q, sc, M, H);
   return cudaGetLastError();
-}
-
-template <bool NORM>
-cudaError_t dispatch_row(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                         int num_sms, unsigned int* fault, cudaStream_t stream) {
-  const int cpw = ((H + 255) / 256 + 7) / 8;
-  switch (cpw) {
-    case 1: return launch_row<NORM, 1>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 2: return launch_row<NORM, 2>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 3: return launch_row<NORM, 3>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 4: return launch_row<NORM, 4>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 5: return launch_row<NORM, 5>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 6: return launch_row<NORM, 6>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 7: return launch_row<NORM, 7>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    case 8: return launch_row<NORM, 8>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 }  // namespace
 
-cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                                 int num_sms, unsigned int* fault, cudaStream_t stream) {
-  return dispatch_row<true>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w), eps, q, sc, M, H,
-                            num_sms, fault, stream);
+// Row ownership: with few rows, 2 or 4 warps share a row so that more loads
+// are in flight; with many rows a warp owns a whole row.
+cudaError_t launch_rmsnorm_quant(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
+                                 int num_sms, unsigned int* /*fault*/, cudaStream_t stream) {
+  const uint16_t* x = static_cast<const uint16_t*>(xv);
+  const uint16_t* w = static_cast<const uint16_t*>(wv);
+  const int nchunk = (H + 255) / 256;
+  const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
+  if (nchunk <= 24 && M >= warps) {
+    if (nchunk <= 4) return launch_norm<1, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
+    if (nchunk <= 8) return launch_norm<1, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
+    if (nchunk <= 16) return launch_norm<1, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
+    return launch_norm<1, 24>(x, w, eps, q, sc, M, H, num_sms, stream);
+  }
+  if (nchunk <= 32 && M >= warps / 2) return launch_norm<2, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
+  if (nchunk <= 32) return launch_norm<4, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
+  return launch_norm<4, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
 }
 
 cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
-                         unsigned int* fault, cudaStream_t stream) {
-  return dispatch_row<false>(static_cast<const uint16_t*>(x), nullptr, 0.0f, q, sc, rows, cols, num_sms, fault,
-                             stream);
+                         unsigned int* /*fault*/, cudaStream_t stream) {
+  const int nchunk = (cols + 255) / 256;
+  const long long tasks = static_cast<long long>(rows) * ((nchunk + 7) / 8) + 127;
+  long long grid = 2LL * num_sms;
+  const long long need = (tasks + ROW_WARPS - 1) / ROW_WARPS;
+  if (grid > need) grid = need;
+  k_quant<8><<<static_cast<unsigned>(grid), ROW_THREADS, 0, stream>>>(static_cast<const uint16_t*>(x), q, sc, rows,
+                                                                      cols);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- probe
