@@ -73,6 +73,20 @@ def gemm_bytes(m, n, k):
     return m * k + sa + n * k + sb + 2 * m * n
 
 
+def aggregate_over_ranks(ms_per_step, work_per_step, world, device=None):
+    """Weak scaling: every rank did `work_per_step` per step; the job's step
+    time is the slowest rank's.  Returns (max ms per step, whole-job work per
+    second).  A rank-independent collective on the timing only; the data path
+    has none."""
+    import torch
+    ms_max = float(ms_per_step)
+    if world > 1:
+        t = torch.tensor([ms_max], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, world * work_per_step / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -224,23 +238,23 @@ def run_gpu(args, rank, world):
 
     # The K timed steps are captured once as a CUDA graph (the launches go
     # through the same C entry points; the graph removes the host's per-call
-    # launch latency, as a serving engine's CUDA-graph mode does).  A second
-    # graph of the same K steps carries timing events between the kernels for
-    # the per-kernel breakdown.
+    # launch latency, as a serving engine's CUDA-graph mode does).  For the
+    # per-kernel breakdown each kernel of the step also gets a graph of its K
+    # launches over the same rotating buffers, timed the same way.
     g_main = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_main, stream=stream):
         for i in range(args.steps):
             step(i)
-    in_graph_events = True
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_marks)]
-               for _ in range(args.steps)]
-        g_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_ev, stream=stream):
+    order = ["norm_quant"]
+    for k in ks:
+        order += [f"quant_a{k}", f"gemm_k{k}"]
+    g_kern = []
+    for idx in range(len(order)):
+        gk = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gk, stream=stream):
             for i in range(args.steps):
-                step(i, evs[i])
-    except TypeError:
-        in_graph_events = False
+                one_kernel(i, idx)
+        g_kern.append(gk)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
@@ -269,36 +283,18 @@ def run_gpu(args, rank, world):
     t_wall1 = time.time()
     total_ms = e0.elapsed_time(e1)
 
-    # per-kernel durations over the same K steps (events inside the graph, or
-    # one graph of K back-to-back launches per kernel if events cannot be
-    # captured by this torch)
-    order = ["norm_quant"]
-    for k in ks:
-        order += [f"quant_a{k}", f"gemm_k{k}"]
-    per_kernel = {name: 0.0 for name in order}
+    # per-kernel durations: each kernel's graph of K launches, replayed once
+    per_kernel = {}
     with torch.cuda.stream(stream):
-        if in_graph_events:
-            g_ev.replay()
+        for idx, name in enumerate(order):
+            b0 = torch.cuda.Event(enable_timing=True)
+            b1 = torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            g_kern[idx].replay()
+            b1.record(stream)
             stream.synchronize()
-            for e in evs:
-                for idx, name in enumerate(order):
-                    per_kernel[name] += e[idx].elapsed_time(e[idx + 1])
-            breakdown_ms = evs[0][0].elapsed_time(evs[-1][n_marks - 1])
-        else:
-            breakdown_ms = 0.0
-            for idx, name in enumerate(order):
-                gk = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gk, stream=stream):
-                    for i in range(args.steps):
-                        one_kernel(i, idx)
-                b0 = torch.cuda.Event(enable_timing=True)
-                b1 = torch.cuda.Event(enable_timing=True)
-                b0.record(stream)
-                gk.replay()
-                b1.record(stream)
-                stream.synchronize()
-                per_kernel[name] = b0.elapsed_time(b1)
-                breakdown_ms += per_kernel[name]
+            per_kernel[name] = b0.elapsed_time(b1)
+    breakdown_ms = sum(per_kernel.values())
     torch.cuda.synchronize()
     sampler.stop()
     assert mx.mx_device_fault() == 0
@@ -311,13 +307,7 @@ def run_gpu(args, rank, world):
     e2e = run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks)
 
     # ---- aggregate over ranks: max time, sum of work
-    times = [ms_per_step]
-    if world > 1:
-        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        times = [float(t.item())]
-    ms_max = times[0]
-    value = world * flops_step / (ms_max * 1e-3) / 1e12
+    ms_max, value = aggregate_over_ranks(ms_per_step, flops_step / 1e12, world, dev)
 
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
@@ -325,7 +315,7 @@ def run_gpu(args, rank, world):
     nq_ms = per_kernel["norm_quant"] / args.steps
     nq_gbs = norm_quant_bytes(M) / (nq_ms * 1e-3) / 1e9
     kern = {}
-    denom = breakdown_ms if breakdown_ms > 0 else total_ms
+    denom = breakdown_ms
     for name in order:
         ms = per_kernel[name] / args.steps
         if name == "norm_quant":
@@ -376,8 +366,8 @@ def run_gpu(args, rank, world):
         "e2e": e2e,
         "gpu_launches": len(order) * args.steps,
         "timing": {"timed_region": "one CUDA-graph replay of the K steps (CUDA events on the launch stream)",
-                   "per_kernel": "timing events inside a second graph of the same K steps" if in_graph_events
-                   else "one graph of K back-to-back launches per kernel"},
+                   "per_kernel": "one CUDA graph of the kernel's K launches per kernel (same rotating buffers), "
+                                 "CUDA events on the launch stream; shares are of the sum of these"},
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
@@ -591,12 +581,27 @@ def run_one_kernel(args):
             launch(i)
             evs[i][1].record(stream)
         stream.synchronize()
+        # the same launches captured in a CUDA graph: device time without the
+        # host's launch latency between them
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(args.steps):
+                launch(i)
+        g.replay()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        g.replay()
+        g1.record(stream)
+        stream.synchronize()
     assert mx.mx_device_fault() == 0
     ms = [a.elapsed_time(b) for a, b in evs]
     med = statistics.median(ms)
+    g_us = g0.elapsed_time(g1) / args.steps * 1e3
     out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel != "norm_quant" else None,
            "launches": args.steps, "us_median": med * 1e3, "us_min": min(ms) * 1e3,
-           "rate_median": work / (med * 1e-3), "rate_best": work / (min(ms) * 1e-3), "unit": unit}
+           "rate_median": work / (med * 1e-3), "rate_best": work / (min(ms) * 1e-3),
+           "us_graph": g_us, "rate_graph": work / (g_us * 1e-6), "unit": unit}
     if args.kernel == "gemm":
         out["plan"] = mx.mx_gemm_plan(M, N_OUT, k)
         out["block_n"] = args.block_n or out["plan"]["block_n"]
