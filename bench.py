@@ -565,7 +565,8 @@ def run_one_kernel(args):
 
         def launch(i):
             j = i % R
-            mx.mx_gemm_ex(ops[j][0], ops[j][1], wqs[j][0], wqs[j][1], outs[j], M, N_OUT, k, args.block_n, sptr)
+            mx.mx_gemm_ex(ops[j][0], ops[j][1], wqs[j][0], wqs[j][1], outs[j], M, N_OUT, k, args.tile_m,
+                          args.tile_n, sptr)
         work, unit = gemm_flops(M, N_OUT, k) / 1e12, "TFLOP/s"
     else:
         raise SystemExit(f"unknown --kernel {args.kernel}")
@@ -604,7 +605,7 @@ def run_one_kernel(args):
            "us_graph": g_us, "rate_graph": work / (g_us * 1e-6), "unit": unit}
     if args.kernel == "gemm":
         out["plan"] = mx.mx_gemm_plan(M, N_OUT, k)
-        out["block_n"] = args.block_n or out["plan"]["block_n"]
+        out["tile"] = [args.tile_m, args.tile_n] if args.tile_m else [out["plan"]["tile_m"], out["plan"]["tile_n"]]
     print(json.dumps(out), flush=True)
 
 
@@ -620,7 +621,8 @@ def main():
     ap.add_argument("--kernel", choices=["norm_quant", "quant", "gemm"],
                     help="time one kernel of the path alone (eager launches)")
     ap.add_argument("--k", type=int, default=0, help="--kernel mode: contraction size (default: workload's last)")
-    ap.add_argument("--block-n", type=int, default=0, help="--kernel gemm: force the tile width")
+    ap.add_argument("--tile-m", type=int, default=0, help="--kernel gemm: force the tile (128 or 256 = CTA pair)")
+    ap.add_argument("--tile-n", type=int, default=0, help="--kernel gemm: force the tile width")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -120,17 +120,19 @@ mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s,
                   const uint8_t* b_q, const uint8_t* b_s,
                   void* out, int64_t M, int64_t N, int64_t K, mx_stream_t stream);
 
-/* mx_gemm with the tile width forced: block_n = 0 picks automatically,
- * otherwise one of 64, 128, 192 (MX_ERR_SHAPE otherwise). */
+/* mx_gemm with the output tile forced.  (tile_m, tile_n) = (0, 0) picks
+ * automatically; otherwise tile_m = 128 (one CTA per tile, tile_n 64, 128 or
+ * 192) or tile_m = 256 (a cluster of two CTAs sharing one tcgen05 MMA, each
+ * staging half of the B tile; tile_n 128 or 192).  MX_ERR_SHAPE otherwise. */
 mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s,
                      const uint8_t* b_q, const uint8_t* b_s,
                      void* out, int64_t M, int64_t N, int64_t K,
-                     int block_n, mx_stream_t stream);
+                     int tile_m, int tile_n, mx_stream_t stream);
 
-/* The launch configuration mx_gemm would use on the current device:
- * tile width, pipeline stages and grid size.  Any out-pointer may be NULL. */
-mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K,
-                       int* block_n, int* stages, int* grid);
+/* The launch configuration mx_gemm would use on the current device: output
+ * tile, pipeline stages and grid size (CTAs).  Any out-pointer may be NULL. */
+mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m,
+                       int* tile_n, int* stages, int* grid);
 
 /* Conformance probe for the element encoder the kernels use: out[i] =
  * E4M3(in[i]) with round-to-nearest-even and saturation at +-448, for n

@@ -63,8 +63,8 @@ def lib() -> ctypes.CDLL:
     L.mx_rmsnorm_quant.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, vp]
     L.mx_quant_weights.argtypes = [vp, u8p, u8p, i64, i64, vp]
     L.mx_gemm.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, vp]
-    L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, vp]
-    L.mx_gemm_plan.argtypes = [i64, i64, i64, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, vp]
+    L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.mx_last_cuda_error.argtypes = []
@@ -124,15 +124,17 @@ def mx_gemm(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, stream=None) -> Non
                                     _stream(stream, a_q)))
 
 
-def mx_gemm_ex(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, block_n: int, stream=None) -> None:
+def mx_gemm_ex(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, tile_m: int = 0, tile_n: int = 0,
+               stream=None) -> None:
     _check("mx_gemm_ex", lib().mx_gemm_ex(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K,
-                                          block_n, _stream(stream, a_q)))
+                                          tile_m, tile_n, _stream(stream, a_q)))
 
 
 def mx_gemm_plan(M: int, N: int, K: int):
-    bn, st, gr = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    _check("mx_gemm_plan", lib().mx_gemm_plan(M, N, K, ctypes.byref(bn), ctypes.byref(st), ctypes.byref(gr)))
-    return {"block_n": bn.value, "stages": st.value, "grid": gr.value}
+    tm, tn, st, gr = (ctypes.c_int(0) for _ in range(4))
+    _check("mx_gemm_plan", lib().mx_gemm_plan(M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(st),
+                                              ctypes.byref(gr)))
+    return {"tile_m": tm.value, "tile_n": tn.value, "stages": st.value, "grid": gr.value}
 
 
 def mx_e4m3_encode_f32(inp, out, n: int, stream=None) -> None:
@@ -177,11 +179,11 @@ def quant(x, stream=None):
     return q, s
 
 
-def gemm(a_q, a_s, b_q, b_s, block_n: int = 0, stream=None):
+def gemm(a_q, a_s, b_q, b_s, tile=(0, 0), stream=None):
     """C = A . B^T in bf16 for MXFP8 operands (A: M x K, B: N x K)."""
     import torch
     M, K = a_q.shape
     N = b_q.shape[0]
     out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
-    mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, block_n, stream)
+    mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, tile[0], tile[1], stream)
     return out

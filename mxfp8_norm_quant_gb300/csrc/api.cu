@@ -144,10 +144,12 @@ MX_API mx_status mx_quant_weights(const void* x, uint8_t* out_q, uint8_t* out_sc
 }
 
 MX_API mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s,
-                            void* out, int64_t M, int64_t N, int64_t K, int block_n, mx_stream_t stream) {
+                            void* out, int64_t M, int64_t N, int64_t K, int tile_m, int tile_n,
+                            mx_stream_t stream) {
   mx_status st = check_gemm(M, N, K);
   if (st != MX_OK) return st;
-  if (block_n != 0 && !mxk::gemm_block_n_supported(block_n)) return MX_ERR_SHAPE;
+  const bool autotile = tile_m == 0 && tile_n == 0;
+  if (!autotile && !mxk::gemm_tile_supported(tile_m, tile_n)) return MX_ERR_SHAPE;
   if (M == 0) return MX_OK;
   if (!a_q || !a_s || !b_q || !b_s || !out) return MX_ERR_NULL;
   if (misaligned(a_q) || misaligned(a_s) || misaligned(b_q) || misaligned(b_s) || misaligned(out))
@@ -155,29 +157,30 @@ MX_API mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s, const uint8_
   const DeviceInfo* d = nullptr;
   st = current_device(&d);
   if (st != MX_OK) return st;
-  const int bn = block_n != 0 ? block_n
-                              : mxk::gemm_pick_block_n(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                                       d->num_sms);
+  if (autotile)
+    mxk::gemm_pick_tile(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), d->num_sms, &tile_m, &tile_n);
   return launched(mxk::launch_gemm(a_q, a_s, b_q, b_s, out, static_cast<int>(M), static_cast<int>(N),
-                                   static_cast<int>(K), bn, d->num_sms, d->fault,
+                                   static_cast<int>(K), tile_m, tile_n, d->num_sms, d->fault,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 MX_API mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s, void* out,
                          int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
-  return mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, 0, stream);
+  return mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, 0, 0, stream);
 }
 
-MX_API mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* block_n, int* stages, int* grid) {
+MX_API mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m, int* tile_n, int* stages, int* grid) {
   mx_status st = check_gemm(M, N, K);
   if (st != MX_OK) return st;
   const DeviceInfo* d = nullptr;
   st = current_device(&d);
   if (st != MX_OK) return st;
-  const int bn = mxk::gemm_pick_block_n(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), d->num_sms);
-  if (block_n) *block_n = bn;
-  if (stages) *stages = mxk::gemm_stages(bn);
-  if (grid) *grid = M == 0 ? 0 : mxk::gemm_grid(static_cast<int>(M), static_cast<int>(N), bn, d->num_sms);
+  int tm = 0, tn = 0;
+  mxk::gemm_pick_tile(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), d->num_sms, &tm, &tn);
+  if (tile_m) *tile_m = tm;
+  if (tile_n) *tile_n = tn;
+  if (stages) *stages = mxk::gemm_stages(tm, tn);
+  if (grid) *grid = M == 0 ? 0 : mxk::gemm_grid(static_cast<int>(M), static_cast<int>(N), tm, tn, d->num_sms);
   return MX_OK;
 }
 

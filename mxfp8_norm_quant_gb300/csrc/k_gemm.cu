@@ -7,28 +7,42 @@
 // with operands whose scales are already in the F8_128x4 layout (PR #64659,
 // Details / "GEMM-RS with a quantized input").
 //
-// Kernel structure (one persistent CTA per SM, 6 warps):
-//   warp 0       TMA producer: per 128-wide K step, a 128x128 E4M3 tile of A
-//                and a BNx128 tile of B (tensor maps, 128-byte swizzle), plus
-//                the 512-byte F8_128x4 scale blocks of A and B (bulk copies)
-//                into a ring of STAGES shared-memory stages;
-//   warp 1       TMEM owner and MMA issuer: copies the stage's scales into
-//                TMEM (tcgen05.cp 32x128b.warpx4) and issues four
-//                tcgen05.mma.kind::mxf8f6f4.block_scale (K=32 each, scale
-//                byte k of each 4-byte TMEM cell) into one of two TMEM
-//                accumulators; tcgen05.commit frees the stage;
-//   warps 2-5    epilogue: TMEM -> registers (tcgen05.ld 32x32b), fp32 ->
-//                bf16 (RNE), stores; then hand the accumulator back.
-// Two accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.  Tiles are dealt round-robin over the persistent CTAs, N-tile
-// fastest, so concurrently running CTAs share A rows and all of B in L2.
+// One kernel template, two tile families:
+//   * PAIR = false: 128 x BN tiles, one CTA per tile;
+//   * PAIR = true:  256 x BN tiles, a cluster of two CTAs running one
+//     cta_group::2 MMA; CTA r stages rows [128 r, +128) of the A tile and
+//     rows [BN/2 r, +BN/2) of the B tile, i.e. half of B per SM.
+// Persistent grid (one CTA per SM), 10 warps per CTA:
+//   warp 0     TMA producer: per K step of 128, the E4M3 tiles of A and B
+//              (tensor maps, 128-byte swizzle) and the 512-byte F8_128x4 scale
+//              blocks of A (one) and B (two consecutive) into a ring of
+//              STAGES shared-memory stages;
+//   warps 6-9  scale warps, one per TMEM lane quarter: move a stage's scale
+//              blocks from shared memory into that stage's TMEM scale slot
+//              with tcgen05.st (keeping the tensor pipe free of scale copies,
+//              which cost it ~200 cycles each when issued as tcgen05.cp);
+//   warp 1     TMEM owner and (leader CTA) MMA issuer: once a stage's scales
+//              are in TMEM (in both CTAs of a pair), four
+//              tcgen05.mma.kind::mxf8f6f4.block_scale (K=32 each, scale byte
+//              k of each 4-byte TMEM cell) into one of two TMEM accumulators;
+//              tcgen05.commit frees the stage (in both CTAs of a pair);
+//   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld 32x32b), fp32 -> bf16
+//              (RNE), 32-byte stores; then hand the accumulator back.
+// Two accumulators let the epilogue of one tile overlap the main loop of the
+// next.  Tiles are dealt round-robin, N-tile fastest, so concurrently running
+// CTAs share A rows and all of B in L2.  In a pair each CTA's copies complete
+// on its own barriers; both CTAs' scale warps report each stage to the
+// leader, and both CTAs' epilogues hand their accumulator back to it.
 //
-// F8_128x4 and TMEM: a 512-byte scale block (128 rows x 4 scale columns,
-// byte (r%32)*16 + (r/32)*4 + c) copied with 32x128b.warpx4 puts rows
-// 32j..32j+31 in TMEM column j, scale column c in byte c of the cell.  A
-// tile whose first row is 32*o rows into a block therefore reads its scales
-// from column offset o, which is how B tiles narrower than 128 rows or not
-// aligned to 128 rows address their scales.
+// F8_128x4 and TMEM: the MMA reads row r's scales from TMEM column
+// (slot + r/32) of lane r%32 in the lane quarters, scale column c in byte c
+// of the cell: exactly a 512-byte scale block (byte (r%32)*16 + (r/32)*4 + c)
+// whose 16-byte line j is written to lane j of every quarter.  A B tile
+// starting 64 rows into a block therefore reads its scales from column
+// offset 2 (tile widths are multiples of 64: an odd column offset is not a
+// valid scale address).  With cta_group::2 each CTA's TMEM holds the A scales
+// of its own rows and the B scales of the whole tile.
+#include <cmath>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -41,56 +55,56 @@ namespace mxk {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BK = 128;
-constexpr int GEMM_THREADS = 192;
+constexpr int BM = 128;  // rows of A per CTA
+constexpr int BK = 128;  // K elements (= bytes) per pipeline stage
+constexpr int GEMM_THREADS = 320;
 constexpr int TMEM_COLS = 512;
 constexpr int SMEM_BUDGET = 220 * 1024;
+constexpr int SF_COLS = 12;  // TMEM columns per stage: 4 for A's scales, 8 for two blocks of B's
 
-template <int BN>
-struct GemmCfg {
+template <int BN, bool PAIR>
+struct Cfg {
+  static constexpr int TM = PAIR ? 2 * BM : BM;      // output tile rows
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows staged per CTA
   static constexpr int A_BYTES = BM * BK;
-  static constexpr int B_BYTES = BN * BK;
+  static constexpr int B_BYTES = B_ROWS * BK;
   static constexpr int SFA_BYTES = 512;
-  static constexpr int SFB_BYTES = 2 * 512;  // up to two 128-row scale blocks
+  static constexpr int SFB_BYTES = 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SF_COLS = 12;  // TMEM columns per stage: 4 for A, 8 for B
   static constexpr int STAGES_SMEM = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES_TMEM = (TMEM_COLS - 2 * BN) / SF_COLS;
   static constexpr int STAGES_MIN = STAGES_SMEM < STAGES_TMEM ? STAGES_SMEM : STAGES_TMEM;
-  static constexpr int STAGES = STAGES_MIN > 8 ? 8 : STAGES_MIN;
+  static constexpr int STAGES = STAGES_MIN > 10 ? 10 : STAGES_MIN;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-  // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], final
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  // full[STAGES], empty[STAGES], sf_ready[STAGES], tmem_full[2], tmem_empty[2], final[2]
+  static constexpr int NUM_BARS = 3 * STAGES + 6;
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 8;
   static constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;  // + slack to align the base to 1 KB
   static constexpr int TMEM_SF = 2 * BN;
-  static_assert(STAGES >= 2, "pipeline too shallow");
+  static_assert(STAGES >= 3, "pipeline too shallow");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 192, "tile width");
   static_assert(B_BYTES % 1024 == 0, "B tiles keep the 1 KB swizzle-atom alignment");
 };
 
 struct GemmArgs {
-  const uint8_t* sfa;
-  const uint8_t* sfb;
   uint16_t* out;
   int M, N, K;
-  int tiles_m, tiles_n, k_tiles;
-  int sfb_blocks;  // ceil(N / 128)
+  int tiles_m, tiles_n, k_tiles;  // tiles_m counts output tiles of Cfg::TM rows
+  int out_32b_aligned;            // 32-byte vector stores are allowed
   unsigned int* fault;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
 // bits 4-5 B scale id, 7-9 A type (0 = E4M3), 10-12 B type, 15/16 K-major,
 // 17-22 N>>3, 23 scale type (1 = UE8M0), 24-28 M>>4, 29-30 A scale id.
-__host__ __device__ constexpr uint32_t idesc_mxf8(int bn, int sf_id) {
-  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(bn >> 3) << 17) | (1u << 23) |
-         (static_cast<uint32_t>(BM >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
@@ -98,55 +112,72 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ int sfb_atoms(int n0, int bn, int sfb_blocks) {
-  const int need = ((n0 & 127) + bn + 127) >> 7;
-  const int have = sfb_blocks - (n0 >> 7);
-  return need < have ? need : have;
+__device__ __forceinline__ void st_global_32B(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_mxf8(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                 const GemmArgs p) {
-  using Cfg = GemmCfg<BN>;
-  constexpr int STAGES = Cfg::STAGES;
+  using C = Cfg<BN, PAIR>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_u32);
 
-  const uint32_t sA = base + Cfg::OFF_A, sB = base + Cfg::OFF_B;
-  const uint32_t sSFA = base + Cfg::OFF_SFA, sSFB = base + Cfg::OFF_SFB;
-  const uint32_t bar_full = base + Cfg::OFF_BAR;
+  const uint32_t sA = base + C::OFF_A, sB = base + C::OFF_B;
+  const uint32_t sSFA = base + C::OFF_SFA, sSFB = base + C::OFF_SFB;
+  const uint32_t bar_full = base + C::OFF_BAR;
   const uint32_t bar_empty = bar_full + 8 * STAGES;
-  const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+  const uint32_t bar_sfready = bar_empty + 8 * STAGES;
+  const uint32_t bar_tfull = bar_sfready + 8 * STAGES;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_final = bar_tempty + 16;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_SLOT);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_ABORT);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int num_tiles = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sfready + 8 * s, PAIR ? 1 : 4);  // the leader's scale-copy commit, or the 4 scale warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, 4);
+      mbar_init(bar_tempty + 8 * a, PAIR ? 8 : 4);  // the epilogue warps of every CTA of the tile
     }
     mbar_init(bar_final, 1);
+    mbar_init(bar_final + 8, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) {
+    cluster_sync();  // both CTAs' barriers initialised, TMEM allocated in both
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -155,15 +186,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       prefetch_tensormap(&tmap_a);
       prefetch_tensormap(&tmap_b);
-      const size_t rb = static_cast<size_t>(p.k_tiles) * 512;  // bytes per 128-row scale block
+      prefetch_tensormap(&tmap_sfa);
+      prefetch_tensormap(&tmap_sfb);
+      const uint32_t lead_full = PAIR ? mapa_shared(bar_full, 0) : bar_full;
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
         const int mt = tile / p.tiles_n, nt = tile % p.tiles_n;
-        const int m0 = mt * BM, n0 = nt * BN;
-        const int atom0 = n0 >> 7;
-        const int nat = sfb_atoms(n0, BN, p.sfb_blocks);
-        const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + 512u + 512u * nat;
+        const int m0 = mt * C::TM + static_cast<int>(rank) * BM;
+        const int n0 = nt * BN;
+        const int b0 = n0 + static_cast<int>(rank) * C::B_ROWS;
         for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
@@ -172,33 +204,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = bar_full + 8 * s;
-          mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, kt * BK, m0, fb);
-          tma_load_2d(sB + s * Cfg::B_BYTES, &tmap_b, kt * BK, n0, fb);
-          bulk_g2s(sSFA + s * Cfg::SFA_BYTES, p.sfa + mt * rb + kt * 512, 512, fb);
-          for (int a = 0; a < nat; ++a)
-            bulk_g2s(sSFB + s * Cfg::SFB_BYTES + a * 512, p.sfb + (atom0 + a) * rb + kt * 512, 512, fb);
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the leader's barrier
+            if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::STAGE_BYTES);
+            const uint32_t fb = lead_full + 8 * s;
+            tma_load_2d_pair(sA + s * C::A_BYTES, &tmap_a, kt * BK, m0, fb);
+            tma_load_2d_pair(sB + s * C::B_BYTES, &tmap_b, kt * BK, b0, fb);
+            tma_load_4d_pair(sSFA + s * C::SFA_BYTES, &tmap_sfa, 0, 0, kt, m0 >> 7, fb);
+            tma_load_4d_pair(sSFB + s * C::SFB_BYTES, &tmap_sfb, 0, 0, kt, n0 >> 7, fb);
+          } else {
+            const uint32_t fb = bar_full + 8 * s;
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            tma_load_2d(sA + s * C::A_BYTES, &tmap_a, kt * BK, m0, fb);
+            tma_load_2d(sB + s * C::B_BYTES, &tmap_b, kt * BK, b0, fb);
+            tma_load_4d(sSFA + s * C::SFA_BYTES, &tmap_sfa, 0, 0, kt, m0 >> 7, fb);
+            tma_load_4d(sSFB + s * C::SFB_BYTES, &tmap_sfb, 0, 0, kt, n0 >> 7, fb);
+          }
         }
       }
-      // every issued copy must land before the CTA may exit (normally a no-op)
-      for (uint32_t s = 0; s < static_cast<uint32_t>(STAGES) && s < it; ++s) {
-        const uint32_t last = s + ((it - 1 - s) / STAGES) * STAGES;
-        if (!mbar_wait(bar_full + 8 * s, (last / STAGES) & 1u, nullptr, DRAIN_LIMIT_NS))
-          atomicOr(p.fault, FAULT_DRAIN);
+      // every issued copy must land before the CTA may exit (normally a no-op);
+      // in a pair the leader's barriers count the copies of both CTAs
+      if (leader) {
+        for (uint32_t s = 0; s < static_cast<uint32_t>(STAGES) && s < it; ++s) {
+          const uint32_t last = s + ((it - 1 - s) / STAGES) * STAGES;
+          if (!mbar_wait(bar_full + 8 * s, (last / STAGES) & 1u, nullptr, DRAIN_LIMIT_NS))
+            atomicOr(p.fault, FAULT_DRAIN);
+        }
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (leader && lane == 0) {
       uint32_t it = 0, tc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tc) {
+      for (int tile = unit; tile < num_tiles && ok; tile += nunits, ++tc) {
         const int nt = tile % p.tiles_n;
-        const int n0 = nt * BN;
-        const int nat = sfb_atoms(n0, BN, p.sfb_blocks);
-        const uint32_t sfb_col = static_cast<uint32_t>((n0 & 127) >> 5);
-        if ((sfb_col & 1u) != 0 || nat > 2) {  // unreachable for BN % 64 == 0; never issue such an MMA
+        const uint32_t sfb_col = static_cast<uint32_t>(((nt * BN) & 127) >> 5);
+        if ((sfb_col & 1u) != 0) {  // unreachable for BN % 64 == 0; never issue such an MMA
           atomicOr(p.fault, FAULT_GEMM_MMA);
           *abort_flag = 1;
           break;
@@ -213,39 +255,118 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t d_tmem = tmem + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+          // the stage's operands have landed and its scales are in TMEM (every CTA of the tile)
+          if (!mbar_wait(bar_sfready + 8 * s, ph, abort_flag)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_t = tmem + Cfg::TMEM_SF + s * Cfg::SF_COLS;
-          const uint32_t sfb_t = sfa_t + 4;
-          tc_cp_32x128b_x4(sfa_t, smem_desc(sSFA + s * Cfg::SFA_BYTES, 0, 128, SWIZZLE_NONE));
-          for (int a = 0; a < nat; ++a)
-            tc_cp_32x128b_x4(sfb_t + 4 * a, smem_desc(sSFB + s * Cfg::SFB_BYTES + a * 512, 0, 128, SWIZZLE_NONE));
-          const uint32_t a_base = sA + s * Cfg::A_BYTES, b_base = sB + s * Cfg::B_BYTES;
+          const uint32_t sfa_t = tmem + C::TMEM_SF + s * SF_COLS;
+          const uint32_t sfb_t = sfa_t + 4 + sfb_col;
+          const uint32_t a_base = sA + s * C::A_BYTES, b_base = sB + s * C::B_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, SWIZZLE_128B);
             const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, SWIZZLE_128B);
-            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BN, k), sfa_t, sfb_t + sfb_col, (kt | k) != 0 ? 1u : 0u);
+            const uint32_t acc_in = (kt | k) != 0 ? 1u : 0u;
+            if constexpr (PAIR) {
+              mma_mxf8_pair(d_tmem, ad, bd, idesc_mxf8(C::TM, BN, k), sfa_t, sfb_t, acc_in);
+            } else {
+              mma_mxf8(d_tmem, ad, bd, idesc_mxf8(C::TM, BN, k), sfa_t, sfb_t, acc_in);
+            }
           }
-          tc_commit(bar_empty + 8 * s);  // stage s is free once these MMAs are done
+          if constexpr (PAIR) {
+            tc_commit_pair_mc(bar_empty + 8 * s, 3);  // stage s is free in both CTAs
+          } else {
+            tc_commit(bar_empty + 8 * s);
+          }
         }
         if (!ok) break;
-        tc_commit(bar_tfull + 8 * acc);  // accumulator ready for the epilogue
+        if constexpr (PAIR) {
+          tc_commit_pair_mc(bar_tfull + 8 * acc, 3);  // accumulators ready in both CTAs
+        } else {
+          tc_commit(bar_tfull + 8 * acc);
+        }
       }
       // no MMA may still be running when TMEM is released
-      tc_commit(bar_final);
+      if constexpr (PAIR) {
+        tc_commit_pair_mc(bar_final, 1);
+      } else {
+        tc_commit(bar_final);
+      }
       if (!mbar_wait(bar_final, 0, nullptr, DRAIN_LIMIT_NS)) atomicOr(p.fault, FAULT_DRAIN);
+    }
+  } else if (warp >= 6 && PAIR) {
+    // -------------------------------------------------------------- scale copies (pair)
+    // one thread of the leader copies each stage's scale blocks from both
+    // CTAs' shared memory into both TMEMs (tcgen05.cp.cta_group::2), apart
+    // from the MMA issuer, and commits to the stage's sf_ready barrier
+    if (leader && warp == 6 && lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
+        for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+            if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t slot = tmem + C::TMEM_SF + s * SF_COLS;
+          tc_cp_32x128b_x4_pair(slot, smem_desc(sSFA + s * C::SFA_BYTES, 0, 128, SWIZZLE_NONE));
+          tc_cp_32x128b_x4_pair(slot + 4, smem_desc(sSFB + s * C::SFB_BYTES, 0, 128, SWIZZLE_NONE));
+          tc_cp_32x128b_x4_pair(slot + 8, smem_desc(sSFB + s * C::SFB_BYTES + 512, 0, 128, SWIZZLE_NONE));
+          tc_commit_pair_mc(bar_sfready + 8 * s, 1);
+        }
+      }
+      tc_commit_pair_mc(bar_final + 8, 1);
+      if (!mbar_wait(bar_final + 8, 0, nullptr, DRAIN_LIMIT_NS)) atomicOr(p.fault, FAULT_DRAIN);
+    }
+  } else if (warp >= 6) {
+    // -------------------------------------------------------------- scale warps
+    // lane j of lane quarter q writes the 16-byte line j of each scale block
+    // to TMEM lane 32q + j: the four quarters hold identical copies
+    const int quad = warp & 3;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint8_t* gSFA = smem + C::OFF_SFA + lane * 16;
+    const uint8_t* gSFB = smem + C::OFF_SFB + lane * 16;
+    uint32_t it = 0;
+    for (int tile = unit; tile < num_tiles; tile += nunits) {
+      bool ok = true;
+      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!warp_wait(bar_full + 8 * s, ph, abort_flag)) {
+          if (lane == 0) {
+            if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        const uint4 va = *reinterpret_cast<const uint4*>(gSFA + s * C::SFA_BYTES);
+        const uint4 vb0 = *reinterpret_cast<const uint4*>(gSFB + s * C::SFB_BYTES);
+        const uint4 vb1 = *reinterpret_cast<const uint4*>(gSFB + s * C::SFB_BYTES + 512);
+        const uint32_t slot = lane_base + C::TMEM_SF + s * SF_COLS;
+        tmem_st_32x32b_x4(slot, va);
+        tmem_st_32x32b_x4(slot + 4, vb0);
+        tmem_st_32x32b_x4(slot + 8, vb1);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfready + 8 * s);
+      }
+      if (!ok) break;
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int quad = warp & 3;  // TMEM lanes this warp may access
+    const int quad = warp & 3;  // the TMEM lane quarter this warp may access
+    const uint32_t lead_tempty = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+    for (int tile = unit; tile < num_tiles; tile += nunits, ++tc) {
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
       if (!warp_wait(bar_tfull + 8 * acc, aph, abort_flag)) {
         if (lane == 0) {
@@ -256,7 +377,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       tc_fence_after();
       const int mt = tile / p.tiles_n, nt = tile % p.tiles_n;
-      const int row = mt * BM + quad * 32 + lane;
+      const int row = mt * C::TM + static_cast<int>(rank) * BM + quad * 32 + lane;
       const int n0 = nt * BN;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
       uint16_t* out_row = p.out + static_cast<size_t>(row) * p.N;
@@ -275,25 +396,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             pk[i].z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
             pk[i].w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(out_row + col);
-          if (col + 32 <= p.N) {
+          uint16_t* dst = out_row + col;
+          if (col + 32 <= p.N && p.out_32b_aligned) {
+            st_global_32B(dst, pk[0], pk[1]);
+            st_global_32B(dst + 16, pk[2], pk[3]);
+          } else if (col + 32 <= p.N) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+            for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(dst)[i] = pk[i];
           } else {
-            for (int i = 0; i < 4 && col + 8 * i < p.N; ++i) dst[i] = pk[i];
+            for (int i = 0; i < 4 && col + 8 * i < p.N; ++i) reinterpret_cast<uint4*>(dst)[i] = pk[i];
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+      if (lane == 0) {
+        if constexpr (PAIR) {
+          mbar_arrive_cluster(lead_tempty + 8 * acc);
+        } else {
+          mbar_arrive(bar_tempty + 8 * acc);
+        }
+      }
     }
   }
 
-  __syncthreads();
+  tc_fence_before();
+  if constexpr (PAIR) {
+    cluster_sync();  // both CTAs done with TMEM and with the leader's barriers
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR) {
+      tmem_dealloc_pair(tmem, TMEM_COLS);
+    } else {
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
   }
 }
 
@@ -328,90 +467,171 @@ cudaError_t make_operand_map(CUtensorMap* map, const uint8_t* ptr, int rows, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// F8_128x4 scale buffer of a (blocks*128) x K operand as a 4-D byte tensor
+// [block][k_tile][4][128]: one box {128, 4, 1, atoms} is `atoms` consecutive
+// 512-byte scale blocks of the same K step (blocks past the end read as 0).
+cudaError_t make_scale_map(CUtensorMap* map, const uint8_t* ptr, int blocks, int k_tiles, int atoms) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {128, 4, static_cast<cuuint64_t>(k_tiles), static_cast<cuuint64_t>(blocks)};
+  const cuuint64_t strides[3] = {128, 512, static_cast<cuuint64_t>(k_tiles) * 512};
+  const cuuint32_t box[4] = {128, 4, 1, static_cast<cuuint32_t>(atoms)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 2;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of two that can be resident at once (cached per device and width).
 template <int BN>
-cudaError_t launch_bn(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
-                      int N, int K, int num_sms, unsigned int* fault, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN>;
-  CUtensorMap ta, tb;
+int pair_max_clusters(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  auto kern = k_gemm_mxf8<BN, true>;
+  using C = Cfg<BN, true>;
+  if (set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES) != cudaSuccess) return num_sms / 2;
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_config(num_sms & ~1, C::SMEM_BYTES, nullptr, &attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <int BN, bool PAIR>
+cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
+                        int N, int K, int num_sms, unsigned int* fault, cudaStream_t stream) {
+  using C = Cfg<BN, PAIR>;
+  CUtensorMap ta, tb, tsa, tsb;
+  const int k_tiles = (K + BK - 1) / BK;
   cudaError_t err = make_operand_map(&ta, aq, M, K, BM);
-  if (err != cudaSuccess) return err;
-  err = make_operand_map(&tb, bq, N, K, BN);
+  if (err == cudaSuccess) err = make_operand_map(&tb, bq, N, K, C::B_ROWS);
+  if (err == cudaSuccess) err = make_scale_map(&tsa, as, (M + 127) / 128, k_tiles, 1);
+  if (err == cudaSuccess) err = make_scale_map(&tsb, bs, (N + 127) / 128, k_tiles, 2);
   if (err != cudaSuccess) return err;
   GemmArgs p;
-  p.sfa = as;
-  p.sfb = bs;
   p.out = static_cast<uint16_t*>(out);
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_m = (M + BM - 1) / BM;
+  p.tiles_m = (M + C::TM - 1) / C::TM;
   p.tiles_n = (N + BN - 1) / BN;
-  p.k_tiles = (K + BK - 1) / BK;
-  p.sfb_blocks = (N + 127) / 128;
+  p.k_tiles = k_tiles;
+  // row pitch 2N is a multiple of 32 (N % 16 == 0) and tile columns start at
+  // multiples of 64 bytes, so the base alone decides
+  p.out_32b_aligned = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.fault = fault;
-  auto kern = k_gemm_mxf8<BN>;
-  err = set_smem_once(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES);
+  auto kern = k_gemm_mxf8<BN, PAIR>;
+  err = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, GEMM_THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
-  return cudaGetLastError();
-}
-
-template <int BN>
-int stages_of() {
-  return GemmCfg<BN>::STAGES;
+  if constexpr (PAIR) {
+    const int clusters = pair_max_clusters<BN>(num_sms);
+    const int pairs = tiles < clusters ? tiles : clusters;
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = pair_config(2 * pairs, C::SMEM_BYTES, stream, &attr);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  } else {
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    kern<<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
-// Tile widths are multiples of 64 so that a tile starts 0 or 64 rows into a
-// 128-row scale block: the B-scale TMEM address is then shifted by 0 or 2
-// columns (an odd column shift is not a valid scale address).
-bool gemm_block_n_supported(int bn) { return bn == 64 || bn == 128 || bn == 192; }
+// Tile shapes: tile_m 128 (one CTA) with tile_n 64/128/192, or tile_m 256 (a
+// CTA pair, cta_group::2) with tile_n 128/192.
+bool gemm_tile_supported(int tile_m, int tile_n) {
+  if (tile_m == 128) return tile_n == 64 || tile_n == 128 || tile_n == 192;
+  if (tile_m == 256) return tile_n == 128 || tile_n == 192;
+  return false;
+}
 
-int gemm_stages(int bn) {
-  switch (bn) {
-    case 64: return stages_of<64>();
-    case 128: return stages_of<128>();
-    case 192: return stages_of<192>();
+int gemm_stages(int tile_m, int tile_n) {
+  if (tile_m == 256) return tile_n == 128 ? Cfg<128, true>::STAGES : tile_n == 192 ? Cfg<192, true>::STAGES : 0;
+  switch (tile_n) {
+    case 64: return Cfg<64, false>::STAGES;
+    case 128: return Cfg<128, false>::STAGES;
+    case 192: return Cfg<192, false>::STAGES;
     default: return 0;
   }
 }
 
-// Tile width from a simple cost model: a 128 x BN x 128 step costs
-// max(2*BN tensor cycles, 128 + BN shared-memory cycles); tiles are dealt in
-// waves of num_sms; a fixed per-tile overhead covers pipeline fill and the
-// last epilogue.
-int gemm_pick_block_n(int M, int N, int K, int num_sms) {
-  static const int cands[] = {64, 128, 192};
-  const long long kt = (K + BK - 1) / BK;
-  long long best = -1;
-  int best_bn = 128;
-  for (int bn : cands) {
-    const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + bn - 1) / bn);
-    const long long waves = (tiles + num_sms - 1) / num_sms;
-    const long long step = 2 * bn > 128 + bn ? 2 * bn : 128 + bn;
-    const long long cost = waves * (kt * step + 800);
-    if (best < 0 || cost < best) {
+// Tile shape from a cost model fitted to measurements of this kernel on
+// GB300: a K step of 128 costs about 600 + 1.2 * tile_n SM cycles whatever
+// the tile family (a fixed per-step cost dominates); tiles are dealt in
+// waves over the SMs (or SM pairs); a fixed per-tile cost covers the
+// pipeline fill and the last epilogue.
+void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n) {
+  struct Cand {
+    int tm, tn;
+  };
+  static const Cand cands[] = {{128, 192}, {256, 192}, {128, 128}, {256, 128}, {128, 64}};
+  const double kt = (K + BK - 1) / BK;
+  double best = -1;
+  int bm = 128, bn = 192;
+  for (const Cand& c : cands) {
+    const bool pair = c.tm == 256;
+    const int units = pair ? num_sms / 2 : num_sms;
+    const double tiles = static_cast<double>((M + c.tm - 1) / c.tm) * ((N + c.tn - 1) / c.tn);
+    const double waves = std::ceil(tiles / units);
+    const double step = 600.0 + 1.2 * c.tn;
+    const double cost = waves * (kt * step + 1500.0);
+    if (best < 0 || cost < best * 0.999) {
       best = cost;
-      best_bn = bn;
+      bm = c.tm;
+      bn = c.tn;
     }
   }
-  return best_bn;
+  *tile_m = bm;
+  *tile_n = bn;
 }
 
-int gemm_grid(int M, int N, int bn, int num_sms) {
-  const int tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+int gemm_grid(int M, int N, int tile_m, int tile_n, int num_sms) {
+  if (tile_m == 256) {
+    const int tiles = ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
+    const int clusters = tile_n == 128 ? pair_max_clusters<128>(num_sms) : pair_max_clusters<192>(num_sms);
+    return 2 * (tiles < clusters ? tiles : clusters);
+  }
+  const int tiles = ((M + BM - 1) / BM) * ((N + tile_n - 1) / tile_n);
   return tiles < num_sms ? tiles : num_sms;
 }
 
 cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
-                        int N, int K, int bn, int num_sms, unsigned int* fault, cudaStream_t stream) {
-  switch (bn) {
-    case 64: return launch_bn<64>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 128: return launch_bn<128>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 192: return launch_bn<192>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+                        int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream) {
+  if (tile_m == 256) {
+    switch (tile_n) {
+      case 128: return launch_tile<128, true>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+      case 192: return launch_tile<192, true>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (tile_n) {
+    case 64: return launch_tile<64, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+    case 128: return launch_tile<128, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+    case 192: return launch_tile<192, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,11 +17,11 @@ cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int c
                          unsigned int* fault, cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, size_t n, int num_sms, cudaStream_t stream);
 
-bool gemm_block_n_supported(int bn);
-int gemm_stages(int bn);
-int gemm_pick_block_n(int M, int N, int K, int num_sms);
-int gemm_grid(int M, int N, int bn, int num_sms);
+bool gemm_tile_supported(int tile_m, int tile_n);
+int gemm_stages(int tile_m, int tile_n);
+void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n);
+int gemm_grid(int M, int N, int tile_m, int tile_n, int num_sms);
 cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
-                        int N, int K, int bn, int num_sms, unsigned int* fault, cudaStream_t stream);
+                        int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream);
 
 }  // namespace mxk

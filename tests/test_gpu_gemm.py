@@ -14,12 +14,16 @@ from mxtest import bf16_bits, gemm_close, np_u8, to_dev
 
 pytestmark = pytest.mark.gpu
 
-BLOCK_NS = [64, 128, 192]
+TILES = [(128, 64), (128, 128), (128, 192), (256, 128), (256, 192)]
 
 
-def _gemm(aq, as_, bq, bs, M, N, K, dev, block_n=0):
+def _tid(t):
+    return "auto" if t == (0, 0) else f"{t[0]}x{t[1]}"
+
+
+def _gemm(aq, as_, bq, bs, M, N, K, dev, tile=(0, 0)):
     out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
-    mx.mx_gemm_ex(to_dev(aq, dev), to_dev(as_, dev), to_dev(bq, dev), to_dev(bs, dev), out, M, N, K, block_n)
+    mx.mx_gemm_ex(to_dev(aq, dev), to_dev(as_, dev), to_dev(bq, dev), to_dev(bs, dev), out, M, N, K, *tile)
     torch.cuda.synchronize()
     assert mx.mx_device_fault() == 0
     return out
@@ -31,13 +35,13 @@ def _random_codes(rng, shape):
     return q
 
 
-@pytest.mark.parametrize("block_n", BLOCK_NS)
-def test_one_hot_b_selects_a_elements(cuda_dev, block_n):
+@pytest.mark.parametrize("tile", TILES, ids=_tid)
+def test_one_hot_b_selects_a_elements(cuda_dev, tile):
     # B row n = E4M3 1.0 at column k_n (scale byte 127): C[m, n] = dec(A)[m, k_n]
     # exactly (4 significant bits fit bf16).  A's scale bytes vary by row and
     # K-block, so a misplaced scale or row fails.
-    rng = np.random.default_rng(block_n)
-    M, N, K = 256, 448, 512
+    rng = np.random.default_rng(tile[0] + tile[1])
+    M, N, K = 384, 448, 512
     aq = _random_codes(rng, (M, K))
     asb = rng.integers(110, 145, size=(M, K // 32), dtype=np.uint8)
     kn = rng.integers(0, K, size=N)
@@ -45,17 +49,17 @@ def test_one_hot_b_selects_a_elements(cuda_dev, block_n):
     bq[np.arange(N), kn] = 0x38
     bsb = np.full((N, K // 32), 127, dtype=np.uint8)
     ref = O.gemm_ref(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb))
-    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, block_n)
+    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, tile)
     expect = torch.from_numpy(ref).float().to(torch.bfloat16)
     assert torch.equal(got.cpu(), expect)
 
 
-@pytest.mark.parametrize("block_n", BLOCK_NS)
-def test_small_integers_exact(cuda_dev, block_n):
+@pytest.mark.parametrize("tile", TILES, ids=_tid)
+def test_small_integers_exact(cuda_dev, tile):
     # entries in {-1, 0, 1} x power-of-two scales that differ per row and
     # K-block of both operands: every partial sum is exact, so the bf16
     # output is the RNE rounding of the exact result, bit for bit.
-    rng = np.random.default_rng(100 + block_n)
+    rng = np.random.default_rng(100 + tile[0] + tile[1])
     M, N, K = 384, 320, 640
     ai = rng.integers(-1, 2, size=(M, K))
     bi = rng.integers(-1, 2, size=(N, K))
@@ -66,7 +70,7 @@ def test_small_integers_exact(cuda_dev, block_n):
     asb = rng.integers(127, 129, size=(M, K // 32), dtype=np.uint8)
     bsb = rng.integers(126, 128, size=(N, K // 32), dtype=np.uint8)
     ref = O.gemm_ref(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb))
-    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, block_n)
+    got = _gemm(aq, O.swizzle_scales(asb), bq, O.swizzle_scales(bsb), M, N, K, cuda_dev, tile)
     expect = torch.from_numpy(ref).float().to(torch.bfloat16)
     assert torch.equal(got.cpu(), expect)
 
@@ -76,14 +80,34 @@ SHAPES = [(128, 6144, 2048), (1, 96, 32), (300, 416, 288), (129, 256, 4096), (51
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-@pytest.mark.parametrize("block_n", [0] + BLOCK_NS)
-def test_random_within_tolerance(cuda_dev, M, N, K, block_n):
+@pytest.mark.parametrize("tile", [(0, 0)] + TILES, ids=_tid)
+def test_random_within_tolerance(cuda_dev, M, N, K, tile):
     a, wt = W.gemm_operands(M, K, seed=M + N + K, n=N)
     aq, as_ = O.quant(bf16_bits(a))
     bq, bs_ = O.quant(bf16_bits(wt))
     ref = O.gemm_ref(aq, as_, bq, bs_)
-    got = _gemm(aq, as_, bq, bs_, M, N, K, cuda_dev, block_n)
+    got = _gemm(aq, as_, bq, bs_, M, N, K, cuda_dev, tile)
     ok, worst = gemm_close(got, ref)
+    assert ok, f"worst err/tol = {worst:.3f}"
+
+
+@pytest.mark.parametrize("tile", [(128, 192), (256, 192)], ids=_tid)
+def test_output_16_byte_aligned_only(cuda_dev, tile):
+    # an output base that is 16- but not 32-byte aligned takes the 16-byte store path
+    M, N, K = 300, 448, 256
+    a, wt = W.gemm_operands(M, K, seed=5, n=N)
+    aq, as_ = O.quant(bf16_bits(a))
+    bq, bs_ = O.quant(bf16_bits(wt))
+    ref = O.gemm_ref(aq, as_, bq, bs_)
+    big = torch.full((M * N + 16,), float("nan"), dtype=torch.bfloat16, device=cuda_dev)
+    base = big.data_ptr()
+    off = 8 if (base + 16) % 32 else 16            # elements: 16 bytes past a 32-byte boundary
+    out = big[off:off + M * N].view(M, N)
+    assert out.data_ptr() % 32 == 16
+    mx.mx_gemm_ex(to_dev(aq, cuda_dev), to_dev(as_, cuda_dev), to_dev(bq, cuda_dev), to_dev(bs_, cuda_dev), out,
+                  M, N, K, *tile)
+    torch.cuda.synchronize()
+    ok, worst = gemm_close(out, ref)
     assert ok, f"worst err/tol = {worst:.3f}"
 
 
@@ -133,4 +157,4 @@ def test_m_sweep_sampled(cuda_dev, m, k):
 def test_plan_is_consistent(cuda_dev):
     for m in W.M_SWEEP:
         p = mx.mx_gemm_plan(m, 6144, 2048)
-        assert p["block_n"] in BLOCK_NS and p["stages"] >= 2 and p["grid"] >= 1
+        assert (p["tile_m"], p["tile_n"]) in TILES and p["stages"] >= 2 and p["grid"] >= 1
