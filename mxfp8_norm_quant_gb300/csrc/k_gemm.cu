@@ -579,26 +579,26 @@ int gemm_stages(int tile_m, int tile_n) {
   }
 }
 
-// Tile shape from a cost model fitted to measurements of this kernel on
-// GB300: a K step of 128 costs about 600 + 1.2 * tile_n SM cycles whatever
-// the tile family (a fixed per-step cost dominates); tiles are dealt in
-// waves over the SMs (or SM pairs); a fixed per-tile cost covers the
+// Tile shape from a cost model of this kernel measured on GB300: the SM
+// cycles one K step of 128 takes in steady state for each tile family (the
+// pair's deeper pipeline makes its steps cheaper per output), tiles dealt in
+// waves over the SMs (or SM pairs), and a fixed per-tile cost for the
 // pipeline fill and the last epilogue.
 void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n) {
   struct Cand {
     int tm, tn;
+    double step;  // cycles per K step of 128, measured
   };
-  static const Cand cands[] = {{128, 192}, {256, 192}, {128, 128}, {256, 128}, {128, 64}};
+  static const Cand cands[] = {{256, 192, 719.0}, {128, 192, 834.0}, {256, 128, 665.0},
+                               {128, 128, 706.0}, {128, 64, 696.0}};
   const double kt = (K + BK - 1) / BK;
   double best = -1;
   int bm = 128, bn = 192;
   for (const Cand& c : cands) {
-    const bool pair = c.tm == 256;
-    const int units = pair ? num_sms / 2 : num_sms;
+    const int units = c.tm == 256 ? num_sms / 2 : num_sms;
     const double tiles = static_cast<double>((M + c.tm - 1) / c.tm) * ((N + c.tn - 1) / c.tn);
     const double waves = std::ceil(tiles / units);
-    const double step = 600.0 + 1.2 * c.tn;
-    const double cost = waves * (kt * step + 1500.0);
+    const double cost = waves * (kt * c.step + 1500.0);
     if (best < 0 || cost < best * 0.999) {
       best = cost;
       bm = c.tm;
