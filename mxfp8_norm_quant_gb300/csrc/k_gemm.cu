@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel of the stream has finished with A, B, their scales and C
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
@@ -483,21 +485,6 @@ cudaError_t make_scale_map(CUtensorMap* map, const uint8_t* ptr, int blocks, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaLaunchConfig_t pair_config(int grid, int smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = 2;
-  attr->val.clusterDim.y = 1;
-  attr->val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
 // Clusters of two that can be resident at once (cached per device and width).
 template <int BN>
 int pair_max_clusters(int num_sms) {
@@ -508,10 +495,9 @@ int pair_max_clusters(int num_sms) {
   auto kern = k_gemm_mxf8<BN, true>;
   using C = Cfg<BN, true>;
   if (set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES) != cudaSuccess) return num_sms / 2;
-  cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = pair_config(num_sms & ~1, C::SMEM_BYTES, nullptr, &attr);
+  LaunchAttrs la(dim3(static_cast<unsigned>(num_sms & ~1)), dim3(GEMM_THREADS), C::SMEM_BYTES, nullptr, 2);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &la.cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -549,13 +535,12 @@ cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq,
   if constexpr (PAIR) {
     const int clusters = pair_max_clusters<BN>(num_sms);
     const int pairs = tiles < clusters ? tiles : clusters;
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = pair_config(2 * pairs, C::SMEM_BYTES, stream, &attr);
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+    LaunchAttrs la(dim3(static_cast<unsigned>(2 * pairs)), dim3(GEMM_THREADS), C::SMEM_BYTES, stream, 2);
+    return cudaLaunchKernelEx(&la.cfg, kern, ta, tb, tsa, tsb, p);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, p);
-    return cudaGetLastError();
+    LaunchAttrs la(dim3(static_cast<unsigned>(grid)), dim3(GEMM_THREADS), C::SMEM_BYTES, stream);
+    return cudaLaunchKernelEx(&la.cfg, kern, ta, tb, tsa, tsb, p);
   }
 }
 

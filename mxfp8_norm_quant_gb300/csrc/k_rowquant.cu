@@ -9,7 +9,7 @@
 // Both kernels are HBM-bound (about 3 bytes per element: 2 read, 1 written)
 // and are built to spend few instructions per element and keep many bytes in
 // flight:
-//   * a row is owned by WPR warps (1, 2 or 4); each lane owns 8 consecutive
+//   * a row is owned by WPR warps (1, 2, 3, 4 or 6); each lane owns 8 consecutive
 //     elements of every 256-element chunk it holds (one 16-byte load per
 //     chunk), and the whole row is loaded into registers with back-to-back
 //     16-byte loads before any arithmetic;
@@ -20,7 +20,8 @@
 //     five tree levels of the chunk), then the tree over the chunks, built
 //     incrementally as a binary counter and closed with zero subtrees; with
 //     WPR > 1 every warp owns an aligned power-of-two run of chunks and the
-//     warp subtotals are added in tree order through shared memory;
+//     warp subtotals are added in tree order (zero-padded to a power of two)
+//     through shared memory;
 //   * 4 lanes hold one 32-element MX block: amax by two shuffles, the UE8M0
 //     byte from the exponent field, one cvt per element pair, an 8-byte
 //     store of codes per lane and one 4-byte store per 4 scales.
@@ -101,16 +102,38 @@ __device__ __forceinline__ void quantize_store(float2 y01, float2 y23, float2 y4
 
 // --------------------------------------------------------------- fused norm
 
+// CTA shape for WPR warps per row: as many whole row groups as fit in 16 warps.
+template <int WPR>
+struct NormCta {
+  static constexpr int GROUPS = ROW_WARPS / WPR;
+  static constexpr int THREADS = GROUPS * WPR * 32;
+};
+
+// Sum of the WPR warp subtotals of a row, in tree order (padded with zeros
+// to a power of two).
+template <int WPR>
+__device__ __forceinline__ float combine_subtotals(const float* t) {
+  if constexpr (WPR == 1) return t[0];
+  if constexpr (WPR == 2) return __fadd_rn(t[0], t[1]);
+  if constexpr (WPR == 3) return __fadd_rn(__fadd_rn(t[0], t[1]), t[2]);
+  if constexpr (WPR == 4) return __fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3]));
+  if constexpr (WPR == 6)
+    return __fadd_rn(__fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3])), __fadd_rn(t[4], t[5]));
+  return 0.0f;
+}
+
 // WPR warps per row, NCH chunks of 256 elements per warp (a power of two when
 // WPR > 1, so that every warp's chunks form an aligned subtree).
 template <int WPR, int NCH>
-__global__ void __launch_bounds__(ROW_THREADS, 1)
+__global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
     k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
                     uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H) {
   static_assert(WPR == 1 || (NCH & (NCH - 1)) == 0, "multi-warp rows need power-of-two chunk runs");
-  constexpr int GROUPS = ROW_WARPS / WPR;
+  static_assert(WPR == 1 || WPR == 2 || WPR == 3 || WPR == 4 || WPR == 6, "warps per row");
+  constexpr int GROUPS = NormCta<WPR>::GROUPS;
+  constexpr int THREADS = NormCta<WPR>::THREADS;
   extern __shared__ float g_s[];  // (1 + w) in fp32, zero-padded to whole chunks
-  __shared__ float red[GROUPS][2][4];
+  __shared__ float red[GROUPS][2][8];
 
   const int nchunk = (H + 255) >> 8;
   const int words = (H / 32 + 3) / 4;
@@ -119,7 +142,9 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   const int grp = warp / WPR, wi = warp % WPR;
   const int c0 = wi * NCH;
 
-  for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
+  pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < nchunk * 256; i += THREADS)
     g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
   __syncthreads();
 
@@ -167,12 +192,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
     if constexpr (WPR > 1) {
       if (lane == 0) red[grp][it & 1][wi] = ss_w;
       named_barrier_sync(1 + grp, WPR * 32);
-      const float* rr = red[grp][it & 1];
-      if constexpr (WPR == 2) {
-        ss = __fadd_rn(rr[0], rr[1]);
-      } else {
-        ss = __fadd_rn(__fadd_rn(rr[0], rr[1]), __fadd_rn(rr[2], rr[3]));
-      }
+      ss = combine_subtotals<WPR>(red[grp][it & 1]);
     }
     // the packed row stays live across the reduction; re-unpacking it in
     // pass 2 is cheaper than keeping every unpacked float alive
@@ -203,6 +223,117 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   }
 }
 
+// One warp per row, with the next row prefetched: each warp owns a
+// shared-memory slot of one row; while it computes the row it holds in
+// registers, a TMA bulk copy brings its next row into the slot, so memory
+// and arithmetic overlap within the warp (the register-only kernel above
+// loads, then computes, then loads again).  NCH * 256 >= H.
+template <int NCH>
+__global__ void __launch_bounds__(ROW_THREADS, 1)
+    k_rmsnorm_quant_pf(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
+                       uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, unsigned int* fault) {
+  extern __shared__ __align__(128) uint8_t smem_pf[];
+  const int nchunk = (H + 255) >> 8;
+  const int slot_bytes = nchunk * 512;
+  float* g_s = reinterpret_cast<float*>(smem_pf);                  // nchunk * 256 floats
+  uint8_t* slots = smem_pf + nchunk * 1024;                        // ROW_WARPS slots
+  const uint32_t bars = smem_u32(slots + ROW_WARPS * slot_bytes);  // one mbarrier per warp
+  const int words = (H / 32 + 3) / 4;
+  const int Mp = ((M + 127) / 128) * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* slot = slots + warp * slot_bytes;
+  const uint32_t slot_s = smem_u32(slot);
+  const uint32_t bar = bars + 8 * warp;
+  const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
+
+  if (lane == 0) mbar_init(bar, 1);
+  fence_barrier_init();
+  pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
+    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
+  __syncthreads();
+
+  const int stride = gridDim.x * ROW_WARPS;
+  int row = blockIdx.x + gridDim.x * warp;
+  if (lane == 0 && row < M) {
+    mbar_arrive_expect_tx(bar, row_bytes);
+    bulk_g2s(slot_s, x + static_cast<size_t>(row) * H, row_bytes, bar);
+  }
+  uint32_t phase = 0;
+  for (; row < Mp; row += stride) {
+    if (row >= M) {
+      // padding row of the last 128-row block: its scale bytes are zero
+      for (int wd = lane; wd < words; wd += 32)
+        *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
+      continue;
+    }
+    if (!warp_wait(bar, phase, nullptr)) {
+      if (lane == 0) atomicOr(fault, FAULT_ROWQ_CONSUMER);
+      break;
+    }
+    phase ^= 1u;
+    uint4 xv[NCH];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int col = j * 256 + lane * 8;
+      xv[j] = col < H ? *reinterpret_cast<const uint4*>(slot + j * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
+    }
+
+    // pass 1: sum of squares, pairwise tree over the row's chunks
+    float lvl[6];
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      float t = warp_tree(lane_square_tree(xv[j]));
+      int k = 0;
+#pragma unroll
+      for (; k < 6; ++k) {
+        if (((j >> k) & 1) == 0) break;
+        t = __fadd_rn(lvl[k], t);
+      }
+      lvl[k] = t;
+    }
+    float ss = 0.0f;
+    bool first = true;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+      if ((NCH >> k) & 1) {
+        ss = first ? lvl[k] : __fadd_rn(lvl[k], ss);
+        first = false;
+      }
+    }
+    // every lane's reads of the slot are consumed: the slot may take the next row
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) asm volatile("" : "+r"(xv[j].x), "+r"(xv[j].y), "+r"(xv[j].z), "+r"(xv[j].w));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    const int next = row + stride;
+    if (lane == 0 && next < M) {
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_g2s(slot_s, x + static_cast<size_t>(next) * H, row_bytes, bar);
+    }
+
+    const float ms = __fdiv_rn(ss, static_cast<float>(H));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    const float2 rr2 = make_float2(r, r);
+    // pass 2: y = (x * r) * (1 + w), then MX quantisation
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      if (j >= nchunk) break;  // warp-uniform
+      const int col = j * 256 + lane * 8;
+      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
+      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
+      const uint4 v = xv[j];
+      const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
+      const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
+      const float2 y45 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr2), make_float2(gb.x, gb.y));
+      const float2 y67 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr2), make_float2(gb.z, gb.w));
+      quantize_store(y01, y23, y45, y67, col < H, lane, row, j, H, words, q, sc);
+      asm volatile("" ::: "memory");
+    }
+  }
+}
+
 // --------------------------------------------------------------- plain quant
 
 // A warp task is up to G consecutive chunks of one row.
@@ -218,6 +349,8 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
   const long long nall = ntask + (Mp - rows);
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * ROW_WARPS;
+  pdl_wait();  // the previous kernel of the stream has finished with x, q and sc
+  pdl_launch_dependents();
   for (long long task = static_cast<long long>(blockIdx.x) * ROW_WARPS + (threadIdx.x >> 5); task < nall;
        task += nwarps) {
     if (task >= ntask) {
@@ -247,6 +380,20 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
   }
 }
 
+template <int NCH>
+cudaError_t launch_norm_pf(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
+                           int num_sms, unsigned int* fault, cudaStream_t stream) {
+  auto kern = k_rmsnorm_quant_pf<NCH>;
+  const int nchunk = (H + 255) / 256;
+  const int smem = nchunk * 1024 + ROW_WARPS * nchunk * 512 + ROW_WARPS * 8;
+  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
+  if (err != cudaSuccess) return err;
+  const int Mp = ((M + 127) / 128) * 128;
+  const int grid = Mp < num_sms ? Mp : num_sms;
+  LaunchAttrs la(dim3(grid), dim3(ROW_THREADS), static_cast<size_t>(smem), stream);
+  return cudaLaunchKernelEx(&la.cfg, kern, x, w, eps, q, sc, M, H, fault);
+}
+
 template <int WPR, int NCH>
 cudaError_t launch_norm(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                         int num_sms, cudaStream_t stream) {
@@ -256,27 +403,38 @@ cudaError_t launch_norm(const uint16_t* x, const uint16_t* w, float eps, uint8_t
   if (err != cudaSuccess) return err;
   const int Mp = ((M + 127) / 128) * 128;
   const int grid = Mp < num_sms ? Mp : num_sms;
-  kern<<<grid, ROW_THREADS, smem, stream>>>(x, w, eps, q, sc, M, H);
-  return cudaGetLastError();
+  LaunchAttrs la(dim3(grid), dim3(NormCta<WPR>::THREADS), static_cast<size_t>(smem), stream);
+  return cudaLaunchKernelEx(&la.cfg, kern, x, w, eps, q, sc, M, H);
 }
 
 }  // namespace
 
-// Row ownership: with few rows, 2 or 4 warps share a row so that more loads
-// are in flight; with many rows a warp owns a whole row.
+// Row ownership: a warp owns a run of chunks (at most 24 x 256 elements in
+// registers); rows wider than one warp's run, and rows in launches with few
+// rows per warp, are split over several warps so that more loads are in
+// flight and each warp's chain is shorter.
 cudaError_t launch_rmsnorm_quant(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                                 int num_sms, unsigned int* /*fault*/, cudaStream_t stream) {
+                                 int num_sms, unsigned int* fault, cudaStream_t stream) {
   const uint16_t* x = static_cast<const uint16_t*>(xv);
   const uint16_t* w = static_cast<const uint16_t*>(wv);
   const int nchunk = (H + 255) / 256;
   const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
-  if (nchunk <= 24 && M >= warps) {
+  const long long rows_per_warp = M / (warps > 0 ? warps : 1);
+  if (nchunk <= 24 && M > warps) {
+    // more than one row per warp: prefetch the next row while computing
+    if (nchunk <= 8) return launch_norm_pf<8>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (nchunk <= 16) return launch_norm_pf<16>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_pf<24>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+  if (nchunk <= 24 && (M >= 512 || rows_per_warp > 0)) {
     if (nchunk <= 4) return launch_norm<1, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
     if (nchunk <= 8) return launch_norm<1, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
     if (nchunk <= 16) return launch_norm<1, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
     return launch_norm<1, 24>(x, w, eps, q, sc, M, H, num_sms, stream);
   }
-  if (nchunk <= 32 && M >= warps / 2) return launch_norm<2, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
+  // a few hundred rows: split each row over several warps to shorten the chain
+  if (nchunk <= 8) return launch_norm<2, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
+  if (nchunk <= 24) return launch_norm<6, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
   if (nchunk <= 32) return launch_norm<4, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
   return launch_norm<4, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
 }
@@ -288,9 +446,8 @@ cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int c
   long long grid = 2LL * num_sms;
   const long long need = (tasks + ROW_WARPS - 1) / ROW_WARPS;
   if (grid > need) grid = need;
-  k_quant<8><<<static_cast<unsigned>(grid), ROW_THREADS, 0, stream>>>(static_cast<const uint16_t*>(x), q, sc, rows,
-                                                                      cols);
-  return cudaGetLastError();
+  LaunchAttrs la(dim3(static_cast<unsigned>(grid)), dim3(ROW_THREADS), 0, stream);
+  return cudaLaunchKernelEx(&la.cfg, k_quant<8>, static_cast<const uint16_t*>(x), q, sc, rows, cols);
 }
 
 // ---------------------------------------------------------------- probe

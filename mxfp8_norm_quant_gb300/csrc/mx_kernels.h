@@ -11,6 +11,34 @@ namespace mxk {
 // current device; the CUDA call is made only when the limit grows.
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
+// Launch attributes shared by every kernel of the library: programmatic
+// stream serialisation (the kernel's set-up overlaps the previous kernel of
+// the stream; the kernels wait on griddepcontrol before touching global
+// memory) and, when cluster_x > 1, the cluster shape.
+struct LaunchAttrs {
+  cudaLaunchAttribute a[2];
+  cudaLaunchConfig_t cfg;
+  LaunchAttrs(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, unsigned cluster_x = 1) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (cluster_x > 1) {
+      a[1].id = cudaLaunchAttributeClusterDimension;
+      a[1].val.clusterDim.x = cluster_x;
+      a[1].val.clusterDim.y = 1;
+      a[1].val.clusterDim.z = 1;
+      n = 2;
+    }
+    cfg.attrs = a;
+    cfg.numAttrs = n;
+  }
+};
+
 cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                                  int num_sms, unsigned int* fault, cudaStream_t stream);
 cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
