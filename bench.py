@@ -58,6 +58,22 @@ def norm_quant_bytes(m, h=H):
     return 2 * m * h + m * h + scale + 2 * h
 
 
+def norm_rowmajor_bytes(m, h=H):
+    """The norm with row-major scales: x read, codes and m * h/32 scale bytes written, w read."""
+    return 2 * m * h + m * h + m * (h // 32) + 2 * h
+
+
+def norm_bf16_bytes(m, h=H):
+    """The norm alone in bf16: x read, y written (2 B/elem each), w read."""
+    return 4 * m * h + 2 * h
+
+
+def swizzle_bytes(m, h=H):
+    """Row-major scales read, the padded F8_128x4 buffer written."""
+    c = h // 32
+    return m * c + (-(-m // 128) * 128) * (-(-c // 4) * 4)
+
+
 def quant_bytes(r, c):
     cs = c // 32
     return 2 * r * c + r * c + (-(-r // 128) * 128) * (-(-cs // 4) * 4)
@@ -548,6 +564,34 @@ def run_one_kernel(args):
         def launch(i):
             mx.mx_rmsnorm_quant(xs[i % R], wd, EPS, qs[i % R], ss[i % R], M, H, sptr)
         work, unit = norm_quant_bytes(M) / 1e9, "GB/s"
+    elif args.kernel in ("norm_rowmajor", "norm_bf16"):
+        x, w = wl.norm()
+        xs = [x.to(dev) for _ in range(R)]
+        wd = w.to(dev)
+        if args.kernel == "norm_bf16":
+            ys = [torch.empty((M, H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+            def launch(i):
+                mx.mx_rmsnorm_bf16(xs[i % R], wd, EPS, ys[i % R], M, H, sptr)
+            work = norm_bf16_bytes(M) / 1e9
+        else:
+            qs = [torch.empty((M, H), dtype=torch.uint8, device=dev) for _ in range(R)]
+            ss = [torch.empty((M, H // 32), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+            def launch(i):
+                mx.mx_rmsnorm_quant_ex(xs[i % R], wd, EPS, qs[i % R], ss[i % R], M, H, mx.MX_SCALES_ROW_MAJOR,
+                                       sptr)
+            work = norm_rowmajor_bytes(M) / 1e9
+        unit = "GB/s"
+    elif args.kernel == "swizzle":
+        x, w = wl.norm()
+        _, s_rm = mx.rmsnorm_quant_rowmajor(x.to(dev), w.to(dev), EPS)
+        ins = [s_rm.clone() for _ in range(R)]
+        outs = [torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+        def launch(i):
+            mx.mx_swizzle_scales(ins[i % R], outs[i % R], M, H, sptr)
+        work, unit = swizzle_bytes(M) / 1e9, "GB/s"
     elif args.kernel == "quant":
         a, _ = wl.gemm(k)
         xs = [a.to(dev) for _ in range(R)]
@@ -599,7 +643,7 @@ def run_one_kernel(args):
     ms = [a.elapsed_time(b) for a, b in evs]
     med = statistics.median(ms)
     g_us = g0.elapsed_time(g1) / args.steps * 1e3
-    out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel != "norm_quant" else None,
+    out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel in ("quant", "gemm") else None,
            "launches": args.steps, "us_median": med * 1e3, "us_min": min(ms) * 1e3,
            "rate_median": work / (med * 1e-3), "rate_best": work / (min(ms) * 1e-3),
            "us_graph": g_us, "rate_graph": work / (g_us * 1e-6), "unit": unit}
@@ -618,7 +662,7 @@ def main():
     ap.add_argument("--workload", default="m1024")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["norm_quant", "quant", "gemm"],
+    ap.add_argument("--kernel", choices=["norm_quant", "norm_rowmajor", "norm_bf16", "swizzle", "quant", "gemm"],
                     help="time one kernel of the path alone (eager launches)")
     ap.add_argument("--k", type=int, default=0, help="--kernel mode: contraction size (default: workload's last)")
     ap.add_argument("--tile-m", type=int, default=0, help="--kernel gemm: force the tile (128 or 256 = CTA pair)")

@@ -100,6 +100,45 @@ mx_status mx_rmsnorm_quant(const void* x, const void* w, float eps,
                            uint8_t* out_q, uint8_t* out_scales,
                            int64_t M, int64_t H, mx_stream_t stream);
 
+/* Scale layouts of mx_rmsnorm_quant_ex. */
+enum {
+  MX_SCALES_F8_128X4 = 0, /* mx_scale_bytes(M, H) bytes, swizzled, as mx_rmsnorm_quant */
+  MX_SCALES_ROW_MAJOR = 1 /* M * (H / 32) bytes, [M][H/32] row-major, no padding      */
+};
+
+/* mx_rmsnorm_quant with the scale layout chosen.  MX_SCALES_ROW_MAJOR serves
+ * sequence parallelism: each rank normalises its own token rows, and the
+ * 128x4-swizzled scales cannot be concatenated by rows after the all-gather,
+ * while row-major ones can; the gathered scales are swizzled once with
+ * mx_swizzle_scales (vLLM PR #65496, Details / Tradeoff).  Codes and scale
+ * values are bit-identical to mx_rmsnorm_quant's.  A row-major scale buffer
+ * needs no alignment (it is written byte by byte); the other pointers must
+ * be 16-byte aligned.  Any other scale_layout: MX_ERR_SHAPE. */
+mx_status mx_rmsnorm_quant_ex(const void* x, const void* w, float eps,
+                              uint8_t* out_q, uint8_t* out_scales,
+                              int64_t M, int64_t H, int scale_layout,
+                              mx_stream_t stream);
+
+/* The Gemma RMSNorm alone: out[M][H] = bf16(y), y as above, rounded to
+ * nearest even.  The path for sequence parallelism in which the norm output
+ * stays BF16 through the all-gather and is quantised afterwards
+ * (mx_quant_weights) (vLLM PR #65496, Overview and Details / Tradeoff).
+ * Same size limits as mx_rmsnorm_quant; out is caller-owned, 16-byte aligned. */
+mx_status mx_rmsnorm_bf16(const void* x, const void* w, float eps, void* out,
+                          int64_t M, int64_t H, mx_stream_t stream);
+
+/* Row-major [rows][cols/32] UE8M0 scales -> the F8_128x4 layout
+ * (mx_scale_bytes(rows, cols) bytes, padding written as 0), and back.
+ * These are the swizzle that runs after the all-gather of row-major scales
+ * (vLLM PR #65496, Details / Tradeoff) and its inverse.  cols is the width of
+ * the quantised operand in elements (cols % 32 == 0, 32 <= cols <= 16384),
+ * rows >= 0.  The row-major buffer needs no alignment; the swizzled one must
+ * be 16-byte aligned.  Input and output must not overlap. */
+mx_status mx_swizzle_scales(const uint8_t* in_row_major, uint8_t* out_swizzled,
+                            int64_t rows, int64_t cols, mx_stream_t stream);
+mx_status mx_unswizzle_scales(const uint8_t* in_swizzled, uint8_t* out_row_major,
+                              int64_t rows, int64_t cols, mx_stream_t stream);
+
 /* Plain MXFP8 quantisation (no norm) of a rows x cols bf16 operand: the
  * activation A (M x K) or the weight W (N x K) of mx_gemm.  Same element and
  * scale rules and the same outputs as mx_rmsnorm_quant with y = x.

@@ -28,9 +28,14 @@ MX_STATUS = {
 }
 
 EXPORTED = (
-    "mx_scale_bytes", "mx_rmsnorm_quant", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+    "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
+    "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
 )
+
+# scale layouts of mx_rmsnorm_quant_ex
+MX_SCALES_F8_128X4 = 0
+MX_SCALES_ROW_MAJOR = 1
 
 
 class MxError(RuntimeError):
@@ -61,6 +66,10 @@ def lib() -> ctypes.CDLL:
     L.mx_scale_bytes.argtypes = [i64, i64]
     L.mx_scale_bytes.restype = ctypes.c_size_t
     L.mx_rmsnorm_quant.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, vp]
+    L.mx_rmsnorm_quant_ex.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, i32, vp]
+    L.mx_rmsnorm_bf16.argtypes = [vp, vp, ctypes.c_float, vp, i64, i64, vp]
+    L.mx_swizzle_scales.argtypes = [u8p, u8p, i64, i64, vp]
+    L.mx_unswizzle_scales.argtypes = [u8p, u8p, i64, i64, vp]
     L.mx_quant_weights.argtypes = [vp, u8p, u8p, i64, i64, vp]
     L.mx_gemm.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, vp]
     L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, vp]
@@ -71,7 +80,8 @@ def lib() -> ctypes.CDLL:
     L.mx_status_string.argtypes = [i32]
     L.mx_status_string.restype = ctypes.c_char_p
     L.mx_version.argtypes = []
-    for name in ("mx_rmsnorm_quant", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+    for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
+                 "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
                  "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -112,6 +122,28 @@ def mx_scale_bytes(rows: int, cols: int) -> int:
 def mx_rmsnorm_quant(x, w, eps: float, out_q, out_scales, M: int, H: int, stream=None) -> None:
     _check("mx_rmsnorm_quant", lib().mx_rmsnorm_quant(_ptr(x), _ptr(w), float(eps), _ptr(out_q), _ptr(out_scales),
                                                       M, H, _stream(stream, x)))
+
+
+def mx_rmsnorm_quant_ex(x, w, eps: float, out_q, out_scales, M: int, H: int, scale_layout: int,
+                        stream=None) -> None:
+    _check("mx_rmsnorm_quant_ex", lib().mx_rmsnorm_quant_ex(_ptr(x), _ptr(w), float(eps), _ptr(out_q),
+                                                            _ptr(out_scales), M, H, scale_layout,
+                                                            _stream(stream, x)))
+
+
+def mx_rmsnorm_bf16(x, w, eps: float, out, M: int, H: int, stream=None) -> None:
+    _check("mx_rmsnorm_bf16", lib().mx_rmsnorm_bf16(_ptr(x), _ptr(w), float(eps), _ptr(out), M, H,
+                                                    _stream(stream, x)))
+
+
+def mx_swizzle_scales(in_row_major, out_swizzled, rows: int, cols: int, stream=None) -> None:
+    _check("mx_swizzle_scales", lib().mx_swizzle_scales(_ptr(in_row_major), _ptr(out_swizzled), rows, cols,
+                                                        _stream(stream, in_row_major)))
+
+
+def mx_unswizzle_scales(in_swizzled, out_row_major, rows: int, cols: int, stream=None) -> None:
+    _check("mx_unswizzle_scales", lib().mx_unswizzle_scales(_ptr(in_swizzled), _ptr(out_row_major), rows, cols,
+                                                            _stream(stream, in_swizzled)))
 
 
 def mx_quant_weights(x, out_q, out_scales, rows: int, cols: int, stream=None) -> None:
@@ -167,6 +199,32 @@ def rmsnorm_quant(x, w, eps: float = 1e-6, stream=None):
     s = torch.empty(mx_scale_bytes(M, H), dtype=torch.uint8, device=x.device)
     mx_rmsnorm_quant(x, w, eps, q, s, M, H, stream)
     return q, s
+
+
+def rmsnorm_quant_rowmajor(x, w, eps: float = 1e-6, stream=None):
+    """Allocates (q, [M][H/32] scales) and runs mx_rmsnorm_quant_ex with row-major scales."""
+    import torch
+    M, H = x.shape
+    q = torch.empty((M, H), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M, H // 32), dtype=torch.uint8, device=x.device)
+    mx_rmsnorm_quant_ex(x, w, eps, q, s, M, H, MX_SCALES_ROW_MAJOR, stream)
+    return q, s
+
+
+def rmsnorm_bf16(x, w, eps: float = 1e-6, stream=None):
+    """Allocates the bf16 output for an (M, H) bf16 CUDA tensor and runs mx_rmsnorm_bf16."""
+    out = x.new_empty(x.shape)
+    mx_rmsnorm_bf16(x, w, eps, out, x.shape[0], x.shape[1], stream)
+    return out
+
+
+def swizzle_scales(s_row_major, cols: int, stream=None):
+    """Allocates the F8_128x4 buffer for (rows, cols/32) row-major scales and runs mx_swizzle_scales."""
+    import torch
+    rows = s_row_major.shape[0]
+    out = torch.empty(mx_scale_bytes(rows, cols), dtype=torch.uint8, device=s_row_major.device)
+    mx_swizzle_scales(s_row_major, out, rows, cols, stream)
+    return out
 
 
 def quant(x, stream=None):

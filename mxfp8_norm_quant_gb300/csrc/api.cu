@@ -129,6 +129,67 @@ MX_API mx_status mx_rmsnorm_quant(const void* x, const void* w, float eps, uint8
                                             d->num_sms, d->fault, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MX_API mx_status mx_rmsnorm_quant_ex(const void* x, const void* w, float eps, uint8_t* out_q, uint8_t* out_scales,
+                                     int64_t M, int64_t H, int scale_layout, mx_stream_t stream) {
+  if (scale_layout == MX_SCALES_F8_128X4) return mx_rmsnorm_quant(x, w, eps, out_q, out_scales, M, H, stream);
+  if (scale_layout != MX_SCALES_ROW_MAJOR) return MX_ERR_SHAPE;
+  mx_status st = check_row_op(M, H);
+  if (st != MX_OK) return st;
+  if (M == 0) return MX_OK;
+  if (!x || !w || !out_q || !out_scales) return MX_ERR_NULL;
+  if (misaligned(x) || misaligned(w) || misaligned(out_q)) return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  return launched(mxk::launch_rmsnorm_quant_rowmajor(x, w, eps, out_q, out_scales, static_cast<int>(M),
+                                                     static_cast<int>(H), d->num_sms, d->fault,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+MX_API mx_status mx_rmsnorm_bf16(const void* x, const void* w, float eps, void* out, int64_t M, int64_t H,
+                                 mx_stream_t stream) {
+  mx_status st = check_row_op(M, H);
+  if (st != MX_OK) return st;
+  if (M == 0) return MX_OK;
+  if (!x || !w || !out) return MX_ERR_NULL;
+  if (misaligned(x) || misaligned(w) || misaligned(out)) return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  return launched(mxk::launch_rmsnorm_bf16(x, w, eps, out, static_cast<int>(M), static_cast<int>(H), d->num_sms,
+                                           d->fault, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+MX_API mx_status mx_swizzle_scales(const uint8_t* in_row_major, uint8_t* out_swizzled, int64_t rows, int64_t cols,
+                                   mx_stream_t stream) {
+  mx_status st = check_row_op(rows, cols);
+  if (st != MX_OK) return st;
+  if (rows == 0) return MX_OK;
+  if (!in_row_major || !out_swizzled) return MX_ERR_NULL;
+  if (misaligned(out_swizzled)) return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  return launched(mxk::launch_swizzle_scales(in_row_major, out_swizzled, static_cast<int>(rows),
+                                             static_cast<int>(cols / 32), d->num_sms,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+MX_API mx_status mx_unswizzle_scales(const uint8_t* in_swizzled, uint8_t* out_row_major, int64_t rows, int64_t cols,
+                                     mx_stream_t stream) {
+  mx_status st = check_row_op(rows, cols);
+  if (st != MX_OK) return st;
+  if (rows == 0) return MX_OK;
+  if (!in_swizzled || !out_row_major) return MX_ERR_NULL;
+  if (misaligned(in_swizzled)) return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  return launched(mxk::launch_unswizzle_scales(in_swizzled, out_row_major, static_cast<int>(rows),
+                                               static_cast<int>(cols / 32), d->num_sms,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MX_API mx_status mx_quant_weights(const void* x, uint8_t* out_q, uint8_t* out_scales, int64_t rows, int64_t cols,
                                   mx_stream_t stream) {
   mx_status st = check_row_op(rows, cols);

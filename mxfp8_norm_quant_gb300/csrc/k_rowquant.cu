@@ -1,338 +1,13 @@
-// Row kernels: fused Gemma RMSNorm + MXFP8 quantisation, and plain MXFP8
-// quantisation of a bf16 operand.
-//
-// The operation is the norm of a decoder layer's input emitting E4M3 data and
-// UE8M0 scales directly (vLLM PR #65496, Overview and Details / Root cause),
-// with the scales in the F8_128x4 layout the GEMM consumes (PR #64659,
-// Details / "GEMM-RS with a quantized input").
-//
-// Both kernels are HBM-bound (about 3 bytes per element: 2 read, 1 written)
-// and are built to spend few instructions per element and keep many bytes in
-// flight:
-//   * a row is owned by WPR warps (1, 2, 3, 4 or 6); each lane owns 8 consecutive
-//     elements of every 256-element chunk it holds (one 16-byte load per
-//     chunk), and the whole row is loaded into registers with back-to-back
-//     16-byte loads before any arithmetic;
-//   * fp32 arithmetic uses the packed f32x2 instructions (two independent
-//     correctly rounded operations each);
-//   * the sum of squares is the pairwise tree exactly: the 8 leaves of a
-//     lane, then a xor-butterfly over the 32 lanes (masks 1..16 are the next
-//     five tree levels of the chunk), then the tree over the chunks, built
-//     incrementally as a binary counter and closed with zero subtrees; with
-//     WPR > 1 every warp owns an aligned power-of-two run of chunks and the
-//     warp subtotals are added in tree order (zero-padded to a power of two)
-//     through shared memory;
-//   * 4 lanes hold one 32-element MX block: amax by two shuffles, the UE8M0
-//     byte from the exponent field, one cvt per element pair, an 8-byte
-//     store of codes per lane and one 4-byte store per 4 scales.
-// No kernel here waits on a barrier other than bar.sync / __syncthreads.
+// Plain MXFP8 quantisation of a bf16 operand, the swizzled-scale form of the
+// fused norm, the standalone scale (un)swizzle kernels and the encoder probe.
+// The norm kernels themselves are in row_common.cuh.
 #include <cstdint>
 
-#include "mx_kernels.h"
-#include "mx_ptx.cuh"
+#include "row_common.cuh"
 
 namespace mxk {
 
 namespace {
-
-constexpr int ROW_WARPS = 16;
-constexpr int ROW_THREADS = ROW_WARPS * 32;
-
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
-
-// byte offset of the 4-scale word (r, 4*wd) in the F8_128x4 layout
-__device__ __forceinline__ size_t scale_word_off(int r, int wd, int words) {
-  return (static_cast<size_t>(r >> 7) * words + wd) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-}
-
-// Pairwise tree of the 8 squares held by one lane:
-// ((e0+e1)+(e2+e3)) + ((e4+e5)+(e6+e7)); the packed pairs (x0,x4), (x1,x5),
-// (x2,x6), (x3,x7) make each packed add one level of the tree.
-__device__ __forceinline__ float lane_square_tree(const uint4& v) {
-  const float2 a = make_float2(bf16lo(v.x), bf16lo(v.z));
-  const float2 b = make_float2(bf16hi(v.x), bf16hi(v.z));
-  const float2 c = make_float2(bf16lo(v.y), bf16lo(v.w));
-  const float2 d = make_float2(bf16hi(v.y), bf16hi(v.w));
-  const float2 l1a = __fadd2_rn(__fmul2_rn(a, a), __fmul2_rn(b, b));  // (e0+e1, e4+e5)
-  const float2 l1b = __fadd2_rn(__fmul2_rn(c, c), __fmul2_rn(d, d));  // (e2+e3, e6+e7)
-  const float2 l2 = __fadd2_rn(l1a, l1b);
-  return __fadd_rn(l2.x, l2.y);
-}
-
-// Tree over the 32 lanes of a warp (lane l holds leaf l); result in all lanes.
-__device__ __forceinline__ float warp_tree(float p) {
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, m));
-  return p;
-}
-
-// Quantises the 8 values a lane holds (4 lanes = one MX block) and stores
-// their codes and, from lanes 0 and 16, the two 4-scale words of the
-// 256-element chunk c of row `row`.
-__device__ __forceinline__ void quantize_store(float2 y01, float2 y23, float2 y45, float2 y67, bool valid,
-                                               int lane, int row, int c, int H, int words, uint8_t* __restrict__ q,
-                                               uint8_t* __restrict__ sc) {
-  float amax = fmaxf(fmaxf(fmaxf(fabsf(y01.x), fabsf(y01.y)), fmaxf(fabsf(y23.x), fabsf(y23.y))),
-                     fmaxf(fmaxf(fabsf(y45.x), fabsf(y45.y)), fmaxf(fabsf(y67.x), fabsf(y67.y))));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const uint32_t byte = ue8m0_from_amax(amax);
-  const float inv = inv_scale_from_ue8m0(byte);
-  const float2 iv = make_float2(inv, inv);
-  const float2 t01 = __fmul2_rn(y01, iv), t23 = __fmul2_rn(y23, iv);
-  const float2 t45 = __fmul2_rn(y45, iv), t67 = __fmul2_rn(y67, iv);
-  uint2 codes;
-  codes.x = cvt_e4m3x2(t01.x, t01.y) | (cvt_e4m3x2(t23.x, t23.y) << 16);
-  codes.y = cvt_e4m3x2(t45.x, t45.y) | (cvt_e4m3x2(t67.x, t67.y) << 16);
-  const int col = c * 256 + lane * 8;
-  if (valid) *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * H + col) = codes;
-  // the four scale bytes of each 128-element word: block b = lane / 4
-  uint32_t wv = valid ? byte << (8 * ((lane >> 2) & 3)) : 0u;
-  wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
-  wv |= __shfl_xor_sync(0xffffffffu, wv, 8);
-  const int wd = 2 * c + (lane >> 4);
-  if ((lane & 15) == 0 && wd < words) *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = wv;
-}
-
-// --------------------------------------------------------------- fused norm
-
-// CTA shape for WPR warps per row: as many whole row groups as fit in 16 warps.
-template <int WPR>
-struct NormCta {
-  static constexpr int GROUPS = ROW_WARPS / WPR;
-  static constexpr int THREADS = GROUPS * WPR * 32;
-};
-
-// Sum of the WPR warp subtotals of a row, in tree order (padded with zeros
-// to a power of two).
-template <int WPR>
-__device__ __forceinline__ float combine_subtotals(const float* t) {
-  if constexpr (WPR == 1) return t[0];
-  if constexpr (WPR == 2) return __fadd_rn(t[0], t[1]);
-  if constexpr (WPR == 3) return __fadd_rn(__fadd_rn(t[0], t[1]), t[2]);
-  if constexpr (WPR == 4) return __fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3]));
-  if constexpr (WPR == 6)
-    return __fadd_rn(__fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3])), __fadd_rn(t[4], t[5]));
-  return 0.0f;
-}
-
-// WPR warps per row, NCH chunks of 256 elements per warp (a power of two when
-// WPR > 1, so that every warp's chunks form an aligned subtree).
-template <int WPR, int NCH>
-__global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
-    k_rmsnorm_quant(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
-                    uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H) {
-  static_assert(WPR == 1 || (NCH & (NCH - 1)) == 0, "multi-warp rows need power-of-two chunk runs");
-  static_assert(WPR == 1 || WPR == 2 || WPR == 3 || WPR == 4 || WPR == 6, "warps per row");
-  constexpr int GROUPS = NormCta<WPR>::GROUPS;
-  constexpr int THREADS = NormCta<WPR>::THREADS;
-  extern __shared__ float g_s[];  // (1 + w) in fp32, zero-padded to whole chunks
-  __shared__ float red[GROUPS][2][8];
-
-  const int nchunk = (H + 255) >> 8;
-  const int words = (H / 32 + 3) / 4;
-  const int Mp = ((M + 127) / 128) * 128;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = warp / WPR, wi = warp % WPR;
-  const int c0 = wi * NCH;
-
-  pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
-  pdl_launch_dependents();
-  for (int i = threadIdx.x; i < nchunk * 256; i += THREADS)
-    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
-  __syncthreads();
-
-  int it = 0;
-  for (int row = blockIdx.x + gridDim.x * grp; row < Mp; row += gridDim.x * GROUPS, ++it) {
-    if (row >= M) {
-      // padding row of the last 128-row block: its scale bytes are zero
-      if (wi == 0)
-        for (int wd = lane; wd < words; wd += 32)
-          *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
-      continue;
-    }
-    const uint16_t* xr = x + static_cast<size_t>(row) * H;
-    uint4 xv[NCH];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int col = (c0 + j) * 256 + lane * 8;
-      xv[j] = col < H ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
-    }
-
-    // pass 1: sum of squares, pairwise tree over the warp's chunks
-    float lvl[6];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      float t = warp_tree(lane_square_tree(xv[j]));
-      int k = 0;
-#pragma unroll
-      for (; k < 6; ++k) {
-        if (((j >> k) & 1) == 0) break;
-        t = __fadd_rn(lvl[k], t);
-      }
-      lvl[k] = t;
-    }
-    // close the tree with zero subtrees: fold the pending subtrees, smallest first
-    float ss_w = 0.0f;
-    bool first = true;
-#pragma unroll
-    for (int k = 0; k < 6; ++k) {
-      if ((NCH >> k) & 1) {
-        ss_w = first ? lvl[k] : __fadd_rn(lvl[k], ss_w);
-        first = false;
-      }
-    }
-    float ss = ss_w;
-    if constexpr (WPR > 1) {
-      if (lane == 0) red[grp][it & 1][wi] = ss_w;
-      named_barrier_sync(1 + grp, WPR * 32);
-      ss = combine_subtotals<WPR>(red[grp][it & 1]);
-    }
-    // the packed row stays live across the reduction; re-unpacking it in
-    // pass 2 is cheaper than keeping every unpacked float alive
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) asm volatile("" : "+r"(xv[j].x), "+r"(xv[j].y), "+r"(xv[j].z), "+r"(xv[j].w));
-    const float ms = __fdiv_rn(ss, static_cast<float>(H));
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    const float2 rr2 = make_float2(r, r);
-
-    // pass 2: y = (x * r) * (1 + w), then MX quantisation
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int c = c0 + j;
-      if (c >= nchunk) break;  // warp-uniform
-      const int col = c * 256 + lane * 8;
-      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
-      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
-      const uint4 v = xv[j];
-      const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
-      const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
-      const float2 y45 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr2), make_float2(gb.x, gb.y));
-      const float2 y67 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr2), make_float2(gb.z, gb.w));
-      quantize_store(y01, y23, y45, y67, col < H, lane, row, c, H, words, q, sc);
-      // keep the next chunk's shared-memory loads from being hoisted above
-      // this point (hoisting them all costs more registers than it hides)
-      asm volatile("" ::: "memory");
-    }
-  }
-}
-
-// One warp per row, with the next row prefetched: each warp owns a
-// shared-memory slot of one row; while it computes the row it holds in
-// registers, a TMA bulk copy brings its next row into the slot, so memory
-// and arithmetic overlap within the warp (the register-only kernel above
-// loads, then computes, then loads again).  NCH * 256 >= H.
-template <int NCH>
-__global__ void __launch_bounds__(ROW_THREADS, 1)
-    k_rmsnorm_quant_pf(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
-                       uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, unsigned int* fault) {
-  extern __shared__ __align__(128) uint8_t smem_pf[];
-  const int nchunk = (H + 255) >> 8;
-  const int slot_bytes = nchunk * 512;
-  float* g_s = reinterpret_cast<float*>(smem_pf);                  // nchunk * 256 floats
-  uint8_t* slots = smem_pf + nchunk * 1024;                        // ROW_WARPS slots
-  const uint32_t bars = smem_u32(slots + ROW_WARPS * slot_bytes);  // one mbarrier per warp
-  const int words = (H / 32 + 3) / 4;
-  const int Mp = ((M + 127) / 128) * 128;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* slot = slots + warp * slot_bytes;
-  const uint32_t slot_s = smem_u32(slot);
-  const uint32_t bar = bars + 8 * warp;
-  const uint32_t row_bytes = 2u * static_cast<uint32_t>(H);
-
-  if (lane == 0) mbar_init(bar, 1);
-  fence_barrier_init();
-  pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
-  pdl_launch_dependents();
-  for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
-    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
-  __syncthreads();
-
-  const int stride = gridDim.x * ROW_WARPS;
-  int row = blockIdx.x + gridDim.x * warp;
-  if (lane == 0 && row < M) {
-    mbar_arrive_expect_tx(bar, row_bytes);
-    bulk_g2s(slot_s, x + static_cast<size_t>(row) * H, row_bytes, bar);
-  }
-  uint32_t phase = 0;
-  for (; row < Mp; row += stride) {
-    if (row >= M) {
-      // padding row of the last 128-row block: its scale bytes are zero
-      for (int wd = lane; wd < words; wd += 32)
-        *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
-      continue;
-    }
-    if (!warp_wait(bar, phase, nullptr)) {
-      if (lane == 0) atomicOr(fault, FAULT_ROWQ_CONSUMER);
-      break;
-    }
-    phase ^= 1u;
-    uint4 xv[NCH];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int col = j * 256 + lane * 8;
-      xv[j] = col < H ? *reinterpret_cast<const uint4*>(slot + j * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
-    }
-
-    // pass 1: sum of squares, pairwise tree over the row's chunks
-    float lvl[6];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      float t = warp_tree(lane_square_tree(xv[j]));
-      int k = 0;
-#pragma unroll
-      for (; k < 6; ++k) {
-        if (((j >> k) & 1) == 0) break;
-        t = __fadd_rn(lvl[k], t);
-      }
-      lvl[k] = t;
-    }
-    float ss = 0.0f;
-    bool first = true;
-#pragma unroll
-    for (int k = 0; k < 6; ++k) {
-      if ((NCH >> k) & 1) {
-        ss = first ? lvl[k] : __fadd_rn(lvl[k], ss);
-        first = false;
-      }
-    }
-    // every lane's reads of the slot are consumed: the slot may take the next row
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) asm volatile("" : "+r"(xv[j].x), "+r"(xv[j].y), "+r"(xv[j].z), "+r"(xv[j].w));
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    const int next = row + stride;
-    if (lane == 0 && next < M) {
-      mbar_arrive_expect_tx(bar, row_bytes);
-      bulk_g2s(slot_s, x + static_cast<size_t>(next) * H, row_bytes, bar);
-    }
-
-    const float ms = __fdiv_rn(ss, static_cast<float>(H));
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    const float2 rr2 = make_float2(r, r);
-    // pass 2: y = (x * r) * (1 + w), then MX quantisation
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      if (j >= nchunk) break;  // warp-uniform
-      const int col = j * 256 + lane * 8;
-      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
-      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
-      const uint4 v = xv[j];
-      const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
-      const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
-      const float2 y45 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr2), make_float2(gb.x, gb.y));
-      const float2 y67 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr2), make_float2(gb.z, gb.w));
-      quantize_store(y01, y23, y45, y67, col < H, lane, row, j, H, words, q, sc);
-      asm volatile("" ::: "memory");
-    }
-  }
-}
 
 // --------------------------------------------------------------- plain quant
 
@@ -373,70 +48,111 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
       const int c = c0 + j;
       if (c >= nchunk) break;  // warp-uniform
       const uint4 v = xv[j];
-      quantize_store(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
+      quantize_store<false>(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
                      make_float2(bf16lo(v.z), bf16hi(v.z)), make_float2(bf16lo(v.w), bf16hi(v.w)),
                      c * 256 + lane * 8 < cols, lane, row, c, cols, words, q, sc);
     }
   }
 }
 
-template <int NCH>
-cudaError_t launch_norm_pf(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                           int num_sms, unsigned int* fault, cudaStream_t stream) {
-  auto kern = k_rmsnorm_quant_pf<NCH>;
-  const int nchunk = (H + 255) / 256;
-  const int smem = nchunk * 1024 + ROW_WARPS * nchunk * 512 + ROW_WARPS * 8;
-  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
-  if (err != cudaSuccess) return err;
-  const int Mp = ((M + 127) / 128) * 128;
-  const int grid = Mp < num_sms ? Mp : num_sms;
-  LaunchAttrs la(dim3(grid), dim3(ROW_THREADS), static_cast<size_t>(smem), stream);
-  return cudaLaunchKernelEx(&la.cfg, kern, x, w, eps, q, sc, M, H, fault);
+// ------------------------------------------------------- scale (un)swizzle
+
+// Row-major [rows][C] scale bytes -> F8_128x4 layout (padding bytes zero).
+// A 128-row block of either layout is one contiguous span (128 * C bytes in,
+// 128 * Cp bytes out), so one CTA permutes one block through shared memory:
+// coalesced loads of the input span into rows of stride S = Cp + 4 bytes (an
+// odd number of words, so the column reads below hit distinct banks), then
+// 16-byte output vectors, each the 4-byte words of rows rl, rl+32, rl+64,
+// rl+96 at one 4-column group, written in output order.
+constexpr int SWZ_THREADS = 256;
+
+__global__ void __launch_bounds__(SWZ_THREADS) k_swizzle_scales(const uint8_t* __restrict__ in,
+                                                                uint8_t* __restrict__ out, int rows, int C) {
+  extern __shared__ __align__(16) uint8_t tile[];
+  const int words = (C + 3) / 4;
+  const int S = words * 4 + 4;
+  const int r0 = blockIdx.x * 128;
+  const int nr = min(128, rows - r0);
+  const uint8_t* src = in + static_cast<size_t>(r0) * C;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int span = nr * C;
+  if ((C & 15) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+    for (int o = threadIdx.x * 16; o < span; o += SWZ_THREADS * 16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + o);
+      uint32_t* d = reinterpret_cast<uint32_t*>(tile + (o / C) * S + o % C);
+      d[0] = v.x;
+      d[1] = v.y;
+      d[2] = v.z;
+      d[3] = v.w;
+    }
+  } else {
+    for (int o = threadIdx.x; o < span; o += SWZ_THREADS) tile[(o / C) * S + o % C] = src[o];
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(blockIdx.x) * words * 512);
+  for (int v = threadIdx.x; v < words * 32; v += SWZ_THREADS) {
+    const int wd = v >> 5, rl = v & 31;
+    uint32_t wv[4];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      const int r = rl + 32 * qd;
+      const uint8_t* t = tile + r * S + 4 * wd;
+      if (r >= nr) {
+        wv[qd] = 0u;
+      } else if (4 * wd + 4 <= C) {
+        wv[qd] = *reinterpret_cast<const uint32_t*>(t);
+      } else {
+        uint32_t b = 0;
+        for (int j = 0; 4 * wd + j < C; ++j) b |= static_cast<uint32_t>(t[j]) << (8 * j);
+        wv[qd] = b;
+      }
+    }
+    dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  }
 }
 
-template <int WPR, int NCH>
-cudaError_t launch_norm(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                        int num_sms, cudaStream_t stream) {
-  auto kern = k_rmsnorm_quant<WPR, NCH>;
-  const int smem = ((H + 255) / 256) * 256 * 4;
-  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
-  if (err != cudaSuccess) return err;
-  const int Mp = ((M + 127) / 128) * 128;
-  const int grid = Mp < num_sms ? Mp : num_sms;
-  LaunchAttrs la(dim3(grid), dim3(NormCta<WPR>::THREADS), static_cast<size_t>(smem), stream);
-  return cudaLaunchKernelEx(&la.cfg, kern, x, w, eps, q, sc, M, H);
+// F8_128x4 layout -> row-major [rows][C] scale bytes, one thread per output byte.
+__global__ void __launch_bounds__(256) k_unswizzle_scales(const uint8_t* __restrict__ in, uint8_t* __restrict__ out,
+                                                          int rows, int C) {
+  const int words = (C + 3) / 4;
+  const long long total = static_cast<long long>(rows) * C;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / C), c = static_cast<int>(i % C);
+    out[i] = in[scale_word_off(r, c >> 2, words) + (c & 3)];
+  }
+}
+
+unsigned scale_grid(long long items, int num_sms) {
+  long long blocks = (items + 255) / 256;
+  const long long cap = 8LL * num_sms;
+  if (blocks > cap) blocks = cap;
+  return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
 }
 
 }  // namespace
 
-// Row ownership: a warp owns a run of chunks (at most 24 x 256 elements in
-// registers); rows wider than one warp's run, and rows in launches with few
-// rows per warp, are split over several warps so that more loads are in
-// flight and each warp's chain is shorter.
-cudaError_t launch_rmsnorm_quant(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
+cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                                  int num_sms, unsigned int* fault, cudaStream_t stream) {
-  const uint16_t* x = static_cast<const uint16_t*>(xv);
-  const uint16_t* w = static_cast<const uint16_t*>(wv);
-  const int nchunk = (H + 255) / 256;
-  const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
-  const long long rows_per_warp = M / (warps > 0 ? warps : 1);
-  if (nchunk <= 24 && M > warps) {
-    // more than one row per warp: prefetch the next row while computing
-    if (nchunk <= 8) return launch_norm_pf<8>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (nchunk <= 16) return launch_norm_pf<16>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_pf<24>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (nchunk <= 24 && (M >= 512 || rows_per_warp > 0)) {
-    if (nchunk <= 4) return launch_norm<1, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (nchunk <= 8) return launch_norm<1, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (nchunk <= 16) return launch_norm<1, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
-    return launch_norm<1, 24>(x, w, eps, q, sc, M, H, num_sms, stream);
-  }
-  // a few hundred rows: split each row over several warps to shorten the chain
-  if (nchunk <= 8) return launch_norm<2, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
-  if (nchunk <= 24) return launch_norm<6, 4>(x, w, eps, q, sc, M, H, num_sms, stream);
-  if (nchunk <= 32) return launch_norm<4, 8>(x, w, eps, q, sc, M, H, num_sms, stream);
-  return launch_norm<4, 16>(x, w, eps, q, sc, M, H, num_sms, stream);
+  return dispatch_norm<OUT_MX_SWIZZLED>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+}
+
+cudaError_t launch_swizzle_scales(const uint8_t* in, uint8_t* out, int rows, int C, int /*num_sms*/,
+                                  cudaStream_t stream) {
+  const int smem = 128 * (((C + 3) / 4) * 4 + 4);
+  cudaError_t err = set_smem_once(reinterpret_cast<const void*>(k_swizzle_scales), smem);
+  if (err != cudaSuccess) return err;
+  LaunchAttrs la(dim3((rows + 127) / 128), dim3(SWZ_THREADS), static_cast<size_t>(smem), stream);
+  return cudaLaunchKernelEx(&la.cfg, k_swizzle_scales, in, out, rows, C);
+}
+
+cudaError_t launch_unswizzle_scales(const uint8_t* in, uint8_t* out, int rows, int C, int num_sms,
+                                    cudaStream_t stream) {
+  LaunchAttrs la(dim3(scale_grid(static_cast<long long>(rows) * C, num_sms)), dim3(256), 0, stream);
+  return cudaLaunchKernelEx(&la.cfg, k_unswizzle_scales, in, out, rows, C);
 }
 
 cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,

@@ -41,8 +41,17 @@ struct LaunchAttrs {
 
 cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                                  int num_sms, unsigned int* fault, cudaStream_t stream);
+// the same norm with row-major [M][H/32] scales, and with a bf16 [M][H] output
+cudaError_t launch_rmsnorm_quant_rowmajor(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M,
+                                          int H, int num_sms, unsigned int* fault, cudaStream_t stream);
+cudaError_t launch_rmsnorm_bf16(const void* x, const void* w, float eps, void* y, int M, int H, int num_sms,
+                                unsigned int* fault, cudaStream_t stream);
 cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
                          unsigned int* fault, cudaStream_t stream);
+// [rows][C] row-major scale bytes <-> the F8_128x4 layout (C = cols / 32)
+cudaError_t launch_swizzle_scales(const uint8_t* in, uint8_t* out, int rows, int C, int num_sms, cudaStream_t stream);
+cudaError_t launch_unswizzle_scales(const uint8_t* in, uint8_t* out, int rows, int C, int num_sms,
+                                    cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, size_t n, int num_sms, cudaStream_t stream);
 
 bool gemm_tile_supported(int tile_m, int tile_n);

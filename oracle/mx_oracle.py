@@ -45,6 +45,9 @@ R6  F8_128x4: the logical scale matrix S[R][C] (C = cols/32) is padded to
                     + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
 R7  GEMM: C = A . B^T with A (M x K) and B (N x K) both K-contiguous; the
     oracle decodes both and multiplies in float64.
+R8  The BF16 form of the norm (the sequence-parallel path of PR #65496, where
+    the norm output stays BF16 through the all-gather and is quantised after
+    it): the fp32 y of R1-R3 rounded to the nearest bf16, ties to even.
 
 The floating-point steps that decide a quantised byte (R2-R5) run in fp32,
 the precision the kernels use; the GEMM reference runs in float64.
@@ -57,6 +60,7 @@ import numpy as np
 __all__ = [
     "BLOCK",
     "bf16_bits_to_f32",
+    "f32_to_bf16_bits",
     "e4m3_decode",
     "e4m3_encode",
     "ue8m0_decode",
@@ -69,6 +73,7 @@ __all__ = [
     "unswizzle_scales",
     "scale_bytes",
     "rmsnorm_quant",
+    "rmsnorm_bf16",
     "quant",
     "mx_decode",
     "gemm_ref",
@@ -87,6 +92,19 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float32, exactly (bf16 is the top half of fp32)."""
     b = np.asarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest, ties to even (R8).
+
+    Dropping the low 16 bits of the fp32 pattern truncates; adding 0x7FFF plus
+    the lowest kept bit first rounds to nearest with ties going to the even
+    pattern (a carry out of the mantissa correctly bumps the exponent).
+    Finite inputs only.
+    """
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    return ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
 
 
 def e4m3_decode(codes: np.ndarray) -> np.ndarray:
@@ -262,6 +280,12 @@ def rmsnorm_quant(x_bits: np.ndarray, w_bits: np.ndarray, eps: float):
     y = gemma_rmsnorm_f32(x_bits, w_bits, eps)
     q, sb = mx_quantize_logical(y)
     return q, swizzle_scales(sb)
+
+
+def rmsnorm_bf16(x_bits: np.ndarray, w_bits: np.ndarray, eps: float) -> np.ndarray:
+    """The Gemma RMSNorm alone, rounded to bf16 (R8).  Returns (M, H) uint16
+    bit patterns."""
+    return f32_to_bf16_bits(gemma_rmsnorm_f32(x_bits, w_bits, eps))
 
 
 def quant(x_bits: np.ndarray):

@@ -87,6 +87,29 @@ def test_quant_rejects(lib):
     assert _status("mx_quant_weights", None, None, None, 0, 64, None) == 0
 
 
+def test_sp_entry_points_reject(lib):
+    f = ctypes.c_float(1e-6)
+    # unknown scale layout; the swizzled layout is mx_rmsnorm_quant itself
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD, GOOD, 4, 64, 2, None) == 3
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD, GOOD, 4, 48, 0, None) == 3
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD, GOOD, 4, 48, 1, None) == 3
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD, None, 4, 64, 1, None) == 1
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD + 8, GOOD, 4, 64, 1, None) == 2
+    assert _status("mx_rmsnorm_quant_ex", GOOD, GOOD, f, GOOD, GOOD + 8, 4, 64, 0, None) == 2
+    assert _status("mx_rmsnorm_quant_ex", None, None, f, None, None, 0, 64, 1, None) == 0
+    assert _status("mx_rmsnorm_bf16", GOOD, GOOD, f, GOOD, 4, 16, None) == 3
+    assert _status("mx_rmsnorm_bf16", GOOD, GOOD, f, None, 4, 64, None) == 1
+    assert _status("mx_rmsnorm_bf16", GOOD, GOOD, f, GOOD + 2, 4, 64, None) == 2
+    for fn in ("mx_swizzle_scales", "mx_unswizzle_scales"):
+        assert _status(fn, GOOD, GOOD, 4, 40, None) == 3
+        assert _status(fn, GOOD, GOOD, -1, 64, None) == 3
+        assert _status(fn, None, GOOD, 4, 64, None) == 1
+        assert _status(fn, GOOD, None, 4, 64, None) == 1
+        assert _status(fn, None, None, 0, 64, None) == 0
+    assert _status("mx_swizzle_scales", GOOD, GOOD + 4, 4, 64, None) == 2
+    assert _status("mx_unswizzle_scales", GOOD + 4, GOOD, 4, 64, None) == 2
+
+
 @pytest.mark.parametrize("M,N,K", [(-1, 6144, 2048), (128, 8, 2048), (128, 6150, 2048), (128, 6144, 48),
                                    (128, 6144, 0), ((1 << 20) + 1, 6144, 2048)])
 def test_gemm_rejects_shapes(lib, M, N, K):

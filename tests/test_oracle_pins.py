@@ -238,6 +238,70 @@ def test_norm_against_float64_definition():
 
 
 # ---------------------------------------------------------------------------
+# BF16 form of the norm (sequence-parallel path)
+# ---------------------------------------------------------------------------
+
+def test_bf16_rounding_hand_values():
+    # bf16 keeps 7 fraction bits: the spacing at 1.0 is 2^-7, so 1 + 2^-8 is a
+    # tie (to even: 1.0) and 1 + 3*2^-8 is a tie (to even: 1 + 2^-6).
+    v = np.array([1.0, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -8 + 2.0 ** -20, -2.5, 3.0e38],
+                 dtype=np.float32)
+    got = O.f32_to_bf16_bits(v)
+    assert got[0] == 0x3F80 and got[1] == 0x3F80 and got[2] == 0x3F82 and got[3] == 0x3F81
+    assert got[4] == 0xC020                                # -2.5 is exact
+    assert got[5] == 0x7F62                                # 0x7F61B1E6: low half above the tie
+
+
+def test_bf16_rounding_matches_torch():
+    # the library cast (round to nearest even) over random finite patterns,
+    # a third of them exact ties
+    rng = np.random.default_rng(17)
+    u = rng.integers(0, 0xFF7FFFFF, size=200_000, dtype=np.uint64).astype(np.uint32)
+    ties = (rng.integers(0, 0x7F7F, size=100_000, dtype=np.uint32) << 16) | 0x8000
+    v = np.concatenate([u, ties, ties | 0x80000000]).view(np.float32)
+    v = v[np.isfinite(v) & (np.abs(v) < 3.38e38)]            # no overflow to inf
+    want = torch.from_numpy(v.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f32_to_bf16_bits(v), want)
+
+
+def test_bf16_rounding_is_nearest():
+    # brute force: the result is the nearer of the two bf16 neighbours
+    rng = np.random.default_rng(19)
+    v = (rng.standard_normal(20_000) * 10.0 ** rng.integers(-30, 30, 20_000)).astype(np.float32)
+    b = O.f32_to_bf16_bits(v)
+    dec = O.bf16_bits_to_f32(b).astype(np.float64)
+    lo = O.bf16_bits_to_f32((v.view(np.uint32) >> 16).astype(np.uint16)).astype(np.float64)
+    hi = O.bf16_bits_to_f32(((v.view(np.uint32) >> 16) + 1).astype(np.uint16)).astype(np.float64)
+    err = np.abs(dec - v.astype(np.float64))
+    assert np.all(err <= np.minimum(np.abs(lo - v), np.abs(hi - v)))
+
+
+def test_rmsnorm_bf16_closed_forms():
+    # x = 2 everywhere, w = 0.5, eps = 0: mean(x^2) = 4, r = 1/2, y = 1.5 (0x3FC0)
+    x = np.full((3, 512), 0x4000, dtype=np.uint16)          # bf16 2.0
+    w = np.full(512, 0x3F00, dtype=np.uint16)               # bf16 0.5
+    assert np.all(O.rmsnorm_bf16(x, w, 0.0) == 0x3FC0)
+    # x = [3, 4, 0...] over H = 32, w = 0, eps = 0: y_0 = 3*sqrt(32)/5 = 3.394...
+    x = np.zeros((1, 32), dtype=np.uint16)
+    x[0, 0], x[0, 1] = 0x4040, 0x4080                       # 3.0, 4.0
+    y = O.bf16_bits_to_f32(O.rmsnorm_bf16(x, np.zeros(32, dtype=np.uint16), 0.0))[0]
+    assert abs(float(y[0]) - 3 * math.sqrt(32) / 5) <= 2.0 ** -7 * 2
+    assert abs(float(y[1]) - 4 * math.sqrt(32) / 5) <= 2.0 ** -7 * 4
+    assert np.all(y[2:] == 0.0)
+
+
+def test_rmsnorm_bf16_within_half_ulp_of_norm():
+    rng = np.random.default_rng(23)
+    xb = _bf16_bits(rng.standard_normal((16, 6144)).astype(np.float32))
+    wb = _bf16_bits(rng.uniform(-0.1, 0.1, 6144).astype(np.float32))
+    y = O.gemma_rmsnorm_f32(xb, wb, 1e-6).astype(np.float64)
+    yb = O.bf16_bits_to_f32(O.rmsnorm_bf16(xb, wb, 1e-6)).astype(np.float64)
+    nz = y != 0
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(y[nz]))) - 7)
+    assert np.all(np.abs(yb[nz] - y[nz]) <= ulp / 2)
+
+
+# ---------------------------------------------------------------------------
 # F8_128x4 layout
 # ---------------------------------------------------------------------------
 
