@@ -601,6 +601,18 @@ def run_one_kernel(args):
         def launch(i):
             mx.mx_quant_weights(xs[i % R], qs[i % R], ss[i % R], M, k, sptr)
         work, unit = quant_bytes(M, k) / 1e9, "GB/s"
+    elif args.kernel == "gemm_quant":
+        a, wt = wl.gemm(k)
+        ops = [mx.quant(a.to(dev)) for _ in range(R)]
+        wqs = [mx.quant(wt.to(dev)) for _ in range(R)]
+        qouts = [torch.empty((M, N_OUT), dtype=torch.uint8, device=dev) for _ in range(R)]
+        souts = [torch.empty(mx.mx_scale_bytes(M, N_OUT), dtype=torch.uint8, device=dev) for _ in range(R)]
+
+        def launch(i):
+            j = i % R
+            mx.mx_gemm_quant(ops[j][0], ops[j][1], wqs[j][0], wqs[j][1], qouts[j], souts[j], M, N_OUT, k,
+                             args.tile_m, args.tile_n, sptr)
+        work, unit = gemm_flops(M, N_OUT, k) / 1e12, "TFLOP/s"
     elif args.kernel == "gemm":
         a, wt = wl.gemm(k)
         ops = [mx.quant(a.to(dev)) for _ in range(R)]
@@ -643,11 +655,11 @@ def run_one_kernel(args):
     ms = [a.elapsed_time(b) for a, b in evs]
     med = statistics.median(ms)
     g_us = g0.elapsed_time(g1) / args.steps * 1e3
-    out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel in ("quant", "gemm") else None,
+    out = {"kernel": args.kernel, "workload": wl.name, "M": M, "K": k if args.kernel in ("quant", "gemm", "gemm_quant") else None,
            "launches": args.steps, "us_median": med * 1e3, "us_min": min(ms) * 1e3,
            "rate_median": work / (med * 1e-3), "rate_best": work / (min(ms) * 1e-3),
            "us_graph": g_us, "rate_graph": work / (g_us * 1e-6), "unit": unit}
-    if args.kernel == "gemm":
+    if args.kernel in ("gemm", "gemm_quant"):
         out["plan"] = mx.mx_gemm_plan(M, N_OUT, k)
         out["tile"] = [args.tile_m, args.tile_n] if args.tile_m else [out["plan"]["tile_m"], out["plan"]["tile_n"]]
     print(json.dumps(out), flush=True)
@@ -662,7 +674,8 @@ def main():
     ap.add_argument("--workload", default="m1024")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["norm_quant", "norm_rowmajor", "norm_bf16", "swizzle", "quant", "gemm"],
+    ap.add_argument("--kernel", choices=["norm_quant", "norm_rowmajor", "norm_bf16", "swizzle", "quant", "gemm",
+                                             "gemm_quant"],
                     help="time one kernel of the path alone (eager launches)")
     ap.add_argument("--k", type=int, default=0, help="--kernel mode: contraction size (default: workload's last)")
     ap.add_argument("--tile-m", type=int, default=0, help="--kernel gemm: force the tile (128 or 256 = CTA pair)")

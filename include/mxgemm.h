@@ -168,6 +168,25 @@ mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s,
                      void* out, int64_t M, int64_t N, int64_t K,
                      int tile_m, int tile_n, mx_stream_t stream);
 
+/* The GEMM with its output quantised in the epilogue: C = A . B^T (fp32
+ * accumulation) is rounded to bf16 (RNE) and leaves the kernel as an MXFP8
+ * operand -- E4M3 codes and UE8M0 scales in the F8_128x4 layout, by the same
+ * rules as mx_quant_weights applied to the bf16 C -- ready to be the A
+ * operand of the next mx_gemm.  This is the shape of a dense GEMM whose
+ * consumer takes a quantized activation (vLLM PR #64659, Details / "GEMM-RS
+ * with a quantized input"; PR #65496, Overview).
+ *
+ *   out_q       [M][N] E4M3 codes, written
+ *   out_scales  mx_scale_bytes(M, N) bytes, written in full (padding 0)
+ *   N % 32 == 0 in addition to mx_gemm's limits; (tile_m, tile_n) as for
+ *   mx_gemm_ex ((0, 0) = automatic).  For a given tile the accumulators, and
+ *   hence the bytes, are those the bf16 mx_gemm_ex of that tile rounds. */
+mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s,
+                        const uint8_t* b_q, const uint8_t* b_s,
+                        uint8_t* out_q, uint8_t* out_scales,
+                        int64_t M, int64_t N, int64_t K,
+                        int tile_m, int tile_n, mx_stream_t stream);
+
 /* The launch configuration mx_gemm would use on the current device: output
  * tile, pipeline stages and grid size (CTAs).  Any out-pointer may be NULL. */
 mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m,

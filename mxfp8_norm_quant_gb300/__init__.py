@@ -29,7 +29,7 @@ MX_STATUS = {
 
 EXPORTED = (
     "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
-    "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+    "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
 )
 
@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
     L.mx_quant_weights.argtypes = [vp, u8p, u8p, i64, i64, vp]
     L.mx_gemm.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, vp]
     L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, vp]
+    L.mx_gemm_quant.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, i64, i64, i64, i32, i32, vp]
     L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -81,7 +82,7 @@ def lib() -> ctypes.CDLL:
     L.mx_status_string.restype = ctypes.c_char_p
     L.mx_version.argtypes = []
     for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
-                 "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_plan",
+                 "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
                  "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -162,6 +163,12 @@ def mx_gemm_ex(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, tile_m: int = 0,
                                           tile_m, tile_n, _stream(stream, a_q)))
 
 
+def mx_gemm_quant(a_q, a_s, b_q, b_s, out_q, out_scales, M: int, N: int, K: int, tile_m: int = 0,
+                  tile_n: int = 0, stream=None) -> None:
+    _check("mx_gemm_quant", lib().mx_gemm_quant(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out_q),
+                                                _ptr(out_scales), M, N, K, tile_m, tile_n, _stream(stream, a_q)))
+
+
 def mx_gemm_plan(M: int, N: int, K: int):
     tm, tn, st, gr = (ctypes.c_int(0) for _ in range(4))
     _check("mx_gemm_plan", lib().mx_gemm_plan(M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(st),
@@ -234,6 +241,17 @@ def quant(x, stream=None):
     q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
     s = torch.empty(mx_scale_bytes(R, C), dtype=torch.uint8, device=x.device)
     mx_quant_weights(x, q, s, R, C, stream)
+    return q, s
+
+
+def gemm_quant(a_q, a_s, b_q, b_s, tile=(0, 0), stream=None):
+    """C = A . B^T leaving as MXFP8 (codes (M, N) uint8, F8_128x4 scales)."""
+    import torch
+    M, K = a_q.shape
+    N = b_q.shape[0]
+    q = torch.empty((M, N), dtype=torch.uint8, device=a_q.device)
+    s = torch.empty(mx_scale_bytes(M, N), dtype=torch.uint8, device=a_q.device)
+    mx_gemm_quant(a_q, a_s, b_q, b_s, q, s, M, N, K, tile[0], tile[1], stream)
     return q, s
 
 

@@ -225,6 +225,29 @@ MX_API mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s, const uint8_
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MX_API mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s,
+                               uint8_t* out_q, uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int tile_m,
+                               int tile_n, mx_stream_t stream) {
+  mx_status st = check_gemm(M, N, K);
+  if (st != MX_OK) return st;
+  if (N % 32 != 0) return MX_ERR_SHAPE;
+  const bool autotile = tile_m == 0 && tile_n == 0;
+  if (!autotile && !mxk::gemm_tile_supported(tile_m, tile_n)) return MX_ERR_SHAPE;
+  if (M == 0) return MX_OK;
+  if (!a_q || !a_s || !b_q || !b_s || !out_q || !out_scales) return MX_ERR_NULL;
+  if (misaligned(a_q) || misaligned(a_s) || misaligned(b_q) || misaligned(b_s) || misaligned(out_q) ||
+      misaligned(out_scales))
+    return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  if (autotile)
+    mxk::gemm_pick_tile(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), d->num_sms, &tile_m, &tile_n);
+  return launched(mxk::launch_gemm_quant(a_q, a_s, b_q, b_s, out_q, out_scales, static_cast<int>(M),
+                                         static_cast<int>(N), static_cast<int>(K), tile_m, tile_n, d->num_sms,
+                                         d->fault, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MX_API mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s, void* out,
                          int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
   return mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, 0, 0, stream);

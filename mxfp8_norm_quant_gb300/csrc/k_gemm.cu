@@ -27,7 +27,13 @@
 //              k of each 4-byte TMEM cell) into one of two TMEM accumulators;
 //              tcgen05.commit frees the stage (in both CTAs of a pair);
 //   warps 2-5  epilogue: TMEM -> registers (tcgen05.ld 32x32b), fp32 -> bf16
-//              (RNE), 32-byte stores; then hand the accumulator back.
+//              (RNE), 32-byte stores; then hand the accumulator back.  In the
+//              MXFP8-output form each thread's 32 columns of one row are one
+//              MX block: the bf16-rounded values are quantised in registers
+//              and stored as 32 E4M3 codes and one UE8M0 byte at its F8_128x4
+//              place, so C leaves the kernel as an MXFP8 operand for the next
+//              GEMM (the quantised-activation output of vLLM PR #64659,
+//              Details / "GEMM-RS with a quantized input").
 // Two accumulators let the epilogue of one tile overlap the main loop of the
 // next.  Tiles are dealt round-robin, N-tile fastest, so concurrently running
 // CTAs share A rows and all of B in L2.  In a pair each CTA's copies complete
@@ -91,8 +97,16 @@ struct Cfg {
   static_assert(B_BYTES % 1024 == 0, "B tiles keep the 1 KB swizzle-atom alignment");
 };
 
+// Output forms of the kernel.
+enum GemmOut : int {
+  GEMM_OUT_BF16 = 0,   // C as bf16
+  GEMM_OUT_MXFP8 = 1,  // C rounded to bf16, then E4M3 codes + F8_128x4 UE8M0 scales
+};
+
 struct GemmArgs {
-  uint16_t* out;
+  uint16_t* out;     // GEMM_OUT_BF16: [M][N] bf16
+  uint8_t* q;        // GEMM_OUT_MXFP8: [M][N] E4M3 codes
+  uint8_t* qs;       // GEMM_OUT_MXFP8: F8_128x4 scales of C, (M, N) operand
   int M, N, K;
   int tiles_m, tiles_n, k_tiles;  // tiles_m counts output tiles of Cfg::TM rows
   int out_32b_aligned;            // 32-byte vector stores are allowed
@@ -118,7 +132,45 @@ __device__ __forceinline__ void st_global_32B(void* p, const uint4& a, const uin
                : "memory");
 }
 
-template <int BN, bool PAIR>
+// One MX block of the output: the 32 accumulators of columns [col, col+32)
+// of `row` rounded to bf16 (RNE), then the shared exponent from their
+// absolute maximum and the 32 E4M3 codes, as the quantisers of the row
+// kernels compute them.  Stores the codes; returns the scale byte.
+__device__ __forceinline__ uint32_t quantize_block_store(const uint32_t (&v)[32], int row, int col, const GemmArgs& p) {
+  float y[32];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint32_t b = pack_bf16x2(v[i], v[i + 1]);
+    y[i] = __uint_as_float(b << 16);
+    y[i + 1] = __uint_as_float(b & 0xFFFF0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
+  const uint32_t byte = ue8m0_from_amax(amax);
+  const float inv = inv_scale_from_ue8m0(byte);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = cvt_e4m3x2(__fmul_rn(y[4 * i], inv), __fmul_rn(y[4 * i + 1], inv)) |
+           (cvt_e4m3x2(__fmul_rn(y[4 * i + 2], inv), __fmul_rn(y[4 * i + 3], inv)) << 16);
+  uint8_t* dst = p.q + static_cast<size_t>(row) * p.N + col;
+  const uint4 lo = make_uint4(w[0], w[1], w[2], w[3]), hi = make_uint4(w[4], w[5], w[6], w[7]);
+  if (p.out_32b_aligned) {
+    st_global_32B(dst, lo, hi);
+  } else {
+    reinterpret_cast<uint4*>(dst)[0] = lo;
+    reinterpret_cast<uint4*>(dst)[1] = hi;
+  }
+  return byte;
+}
+
+// Byte offset of the scale of (row, 32-column block cb) in the F8_128x4 layout.
+__device__ __forceinline__ size_t out_scale_off(int row, int cb, int words) {
+  return (static_cast<size_t>(row >> 7) * words + (cb >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (cb & 3);
+}
+
+template <int BN, bool PAIR, int OUT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_mxf8(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -389,6 +441,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tmem_ld_32x32b_x32(t_row + c, v);
         tmem_ld_wait();
         const int col = n0 + c;
+        if constexpr (OUT == GEMM_OUT_MXFP8) {
+          // N % 32 == 0: a 32-column chunk is in C entirely or not at all
+          const int Mp = (p.M + 127) & ~127;
+          const int blocks = p.N >> 5, words = (blocks + 3) >> 2;
+          if (col < p.N && row < Mp) {
+            const int cb = col >> 5;
+            // a padding row of the last 128-row block gets a zero scale byte
+            const uint32_t byte = row < p.M ? quantize_block_store(v, row, col, p) : 0u;
+            p.qs[out_scale_off(row, cb, words)] = static_cast<uint8_t>(byte);
+            if (cb == blocks - 1)  // padding scale columns of the last 4-column group
+              for (int pc = blocks; pc < 4 * words; ++pc) p.qs[out_scale_off(row, pc, words)] = 0;
+          }
+          continue;
+        }
         if (row < p.M && col < p.N) {
           uint4 pk[4];
 #pragma unroll
@@ -492,7 +558,8 @@ int pair_max_clusters(int num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
-  auto kern = k_gemm_mxf8<BN, true>;
+  // both output forms have the same shared memory and block: one answer serves both
+  auto kern = k_gemm_mxf8<BN, true, GEMM_OUT_BF16>;
   using C = Cfg<BN, true>;
   if (set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES) != cudaSuccess) return num_sms / 2;
   LaunchAttrs la(dim3(static_cast<unsigned>(num_sms & ~1)), dim3(GEMM_THREADS), C::SMEM_BYTES, nullptr, 2);
@@ -505,9 +572,10 @@ int pair_max_clusters(int num_sms) {
   return n;
 }
 
-template <int BN, bool PAIR>
-cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
-                        int N, int K, int num_sms, unsigned int* fault, cudaStream_t stream) {
+template <int BN, bool PAIR, int OUT>
+cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
+                        uint8_t* q, uint8_t* qs, int M, int N, int K, int num_sms, unsigned int* fault,
+                        cudaStream_t stream) {
   using C = Cfg<BN, PAIR>;
   CUtensorMap ta, tb, tsa, tsb;
   const int k_tiles = (K + BK - 1) / BK;
@@ -518,17 +586,21 @@ cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq,
   if (err != cudaSuccess) return err;
   GemmArgs p;
   p.out = static_cast<uint16_t*>(out);
+  p.q = q;
+  p.qs = qs;
   p.M = M;
   p.N = N;
   p.K = K;
   p.tiles_m = (M + C::TM - 1) / C::TM;
   p.tiles_n = (N + BN - 1) / BN;
   p.k_tiles = k_tiles;
-  // row pitch 2N is a multiple of 32 (N % 16 == 0) and tile columns start at
-  // multiples of 64 bytes, so the base alone decides
-  p.out_32b_aligned = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
+  // bf16: row pitch 2N is a multiple of 32 (N % 16 == 0) and tile columns
+  // start at multiples of 64 bytes; codes: row pitch N and chunk columns are
+  // multiples of 32 (N % 32 == 0).  So the base alone decides.
+  const void* vec_base = OUT == GEMM_OUT_MXFP8 ? static_cast<const void*>(q) : out;
+  p.out_32b_aligned = (reinterpret_cast<uintptr_t>(vec_base) & 31u) == 0 ? 1 : 0;
   p.fault = fault;
-  auto kern = k_gemm_mxf8<BN, PAIR>;
+  auto kern = k_gemm_mxf8<BN, PAIR, OUT>;
   err = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const int tiles = p.tiles_m * p.tiles_n;
@@ -604,21 +676,40 @@ int gemm_grid(int M, int N, int tile_m, int tile_n, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
-                        int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream) {
+namespace {
+
+template <int OUT>
+cudaError_t dispatch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
+                          uint8_t* q, uint8_t* qs, int M, int N, int K, int tile_m, int tile_n, int num_sms,
+                          unsigned int* fault, cudaStream_t stream) {
   if (tile_m == 256) {
     switch (tile_n) {
-      case 128: return launch_tile<128, true>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-      case 192: return launch_tile<192, true>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+      case 128: return launch_tile<128, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
+      case 192: return launch_tile<192, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (tile_n) {
-    case 64: return launch_tile<64, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 128: return launch_tile<128, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
-    case 192: return launch_tile<192, false>(aq, as, bq, bs, out, M, N, K, num_sms, fault, stream);
+    case 64: return launch_tile<64, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
+    case 128: return launch_tile<128, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
+    case 192: return launch_tile<192, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
+                        int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream) {
+  return dispatch_tile<GEMM_OUT_BF16>(aq, as, bq, bs, out, nullptr, nullptr, M, N, K, tile_m, tile_n, num_sms, fault,
+                                      stream);
+}
+
+cudaError_t launch_gemm_quant(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, uint8_t* q,
+                              uint8_t* qs, int M, int N, int K, int tile_m, int tile_n, int num_sms,
+                              unsigned int* fault, cudaStream_t stream) {
+  return dispatch_tile<GEMM_OUT_MXFP8>(aq, as, bq, bs, nullptr, q, qs, M, N, K, tile_m, tile_n, num_sms, fault,
+                                       stream);
 }
 
 }  // namespace mxk

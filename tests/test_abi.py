@@ -129,6 +129,21 @@ def test_gemm_null_alignment_and_block_n(lib):
     assert _status("mx_gemm", None, None, None, None, None, 0, 256, 256, None) == 0
 
 
+def test_gemm_quant_rejects(lib):
+    args = [GOOD] * 6
+    assert _status("mx_gemm_quant", *args, 128, 6144 + 16, 2048, 0, 0, None) == 3    # N % 32
+    assert _status("mx_gemm_quant", *args, 128, 6144, 48, 0, 0, None) == 3
+    assert _status("mx_gemm_quant", *args, -1, 6144, 2048, 0, 0, None) == 3
+    assert _status("mx_gemm_quant", *args, 128, 6144, 2048, 256, 64, None) == 3
+    for i in range(6):
+        a = list(args)
+        a[i] = None
+        assert _status("mx_gemm_quant", *a, 128, 256, 256, 0, 0, None) == 1
+        a[i] = GOOD + 8
+        assert _status("mx_gemm_quant", *a, 128, 256, 256, 0, 0, None) == 2
+    assert _status("mx_gemm_quant", None, None, None, None, None, None, 0, 256, 256, 0, 0, None) == 0
+
+
 def test_e4m3_probe_and_fault_reject(lib):
     assert _status("mx_e4m3_encode_f32", GOOD, GOOD, -1, None) == 3
     assert _status("mx_e4m3_encode_f32", None, GOOD, 4, None) == 1
