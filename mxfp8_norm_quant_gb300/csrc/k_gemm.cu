@@ -34,8 +34,10 @@
 //              place, so C leaves the kernel as an MXFP8 operand for the next
 //              GEMM (the quantised-activation output of vLLM PR #64659,
 //              Details / "GEMM-RS with a quantized input").
-// Two accumulators let the epilogue of one tile overlap the main loop of the
-// next.  Tiles are dealt round-robin, N-tile fastest, so concurrently running
+// The single threads that issue copies, scale moves and MMAs are
+// instruction-bound, so their loops keep descriptors as 32-bit words and ring
+// positions as counters.  Two accumulators let the epilogue of one tile
+// overlap the main loop of the next.  Tiles are dealt round-robin, N-tile fastest, so concurrently running
 // CTAs share A rows and all of B in L2.  In a pair each CTA's copies complete
 // on its own barriers; both CTAs' scale warps report each stage to the
 // leader, and both CTAs' epilogues hand their accumulator back to it.
@@ -243,7 +245,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       prefetch_tensormap(&tmap_sfa);
       prefetch_tensormap(&tmap_sfb);
       const uint32_t lead_full = PAIR ? mapa_shared(bar_full, 0) : bar_full;
-      uint32_t it = 0;
+      // stage s and its phase parity ph advance together; `it` counts stages issued
+      uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
         const int mt = tile / p.tiles_n, nt = tile % p.tiles_n;
@@ -251,7 +254,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int n0 = nt * BN;
         const int b0 = n0 + static_cast<int>(rank) * C::B_ROWS;
         for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_PRODUCER);
             *abort_flag = 1;
@@ -274,6 +276,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tma_load_4d(sSFA + s * C::SFA_BYTES, &tmap_sfa, 0, 0, kt, m0 >> 7, fb);
             tma_load_4d(sSFB + s * C::SFB_BYTES, &tmap_sfb, 0, 0, kt, n0 >> 7, fb);
           }
+          if (++s == static_cast<uint32_t>(STAGES)) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       // every issued copy must land before the CTA may exit (normally a no-op);
@@ -289,7 +295,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (leader && lane == 0) {
-      uint32_t it = 0, tc = 0;
+      // the single issuing thread is instruction-bound: descriptors are kept
+      // as 32-bit words advanced by adds, stage and phase by counters
+      const uint32_t a_lo0 = static_cast<uint32_t>(smem_desc(sA, 16, 1024, SWIZZLE_128B));
+      const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc(sB, 16, 1024, SWIZZLE_128B));
+      const uint32_t d_hi = static_cast<uint32_t>(smem_desc(sA, 16, 1024, SWIZZLE_128B) >> 32);
+      uint32_t s = 0, ph = 0, tc = 0;
       bool ok = true;
       for (int tile = unit; tile < num_tiles && ok; tile += nunits, ++tc) {
         const int nt = tile % p.tiles_n;
@@ -307,8 +318,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
-        for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
           // the stage's operands have landed and its scales are in TMEM (every CTA of the tile)
           if (!mbar_wait(bar_sfready + 8 * s, ph, abort_flag)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
@@ -319,22 +329,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t sfa_t = tmem + C::TMEM_SF + s * SF_COLS;
           const uint32_t sfb_t = sfa_t + 4 + sfb_col;
-          const uint32_t a_base = sA + s * C::A_BYTES, b_base = sB + s * C::B_BYTES;
+          const uint32_t a_lo = a_lo0 + s * (C::A_BYTES >> 4), b_lo = b_lo0 + s * (C::B_BYTES >> 4);
+          // K advances 32 bytes (2 descriptor units) per MMA inside the 128-byte swizzled rows
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {
-            const uint64_t ad = smem_desc(a_base + 32 * k, 16, 1024, SWIZZLE_128B);
-            const uint64_t bd = smem_desc(b_base + 32 * k, 16, 1024, SWIZZLE_128B);
-            const uint32_t acc_in = (kt | k) != 0 ? 1u : 0u;
-            if constexpr (PAIR) {
-              mma_mxf8_pair(d_tmem, ad, bd, idesc_mxf8(C::TM, BN, k), sfa_t, sfb_t, acc_in);
-            } else {
-              mma_mxf8(d_tmem, ad, bd, idesc_mxf8(C::TM, BN, k), sfa_t, sfb_t, acc_in);
-            }
-          }
+          for (int k = 0; k < BK / 32; ++k)
+            mma_mxf8_w<PAIR>(d_tmem, a_lo + 2 * k, d_hi, b_lo + 2 * k, d_hi, idesc_mxf8(C::TM, BN, k), sfa_t, sfb_t,
+                             (kt | k) != 0 ? 1u : 0u);
           if constexpr (PAIR) {
             tc_commit_pair_mc(bar_empty + 8 * s, 3);  // stage s is free in both CTAs
           } else {
             tc_commit(bar_empty + 8 * s);
+          }
+          if (++s == static_cast<uint32_t>(STAGES)) {
+            s = 0;
+            ph ^= 1u;
           }
         }
         if (!ok) break;
@@ -358,11 +366,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // CTAs' shared memory into both TMEMs (tcgen05.cp.cta_group::2), apart
     // from the MMA issuer, and commits to the stage's sf_ready barrier
     if (leader && warp == 6 && lane == 0) {
-      uint32_t it = 0;
+      uint32_t s = 0, ph = 0;
       bool ok = true;
       for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
-        for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
             *abort_flag = 1;
@@ -375,6 +382,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tc_cp_32x128b_x4_pair(slot + 4, smem_desc(sSFB + s * C::SFB_BYTES, 0, 128, SWIZZLE_NONE));
           tc_cp_32x128b_x4_pair(slot + 8, smem_desc(sSFB + s * C::SFB_BYTES + 512, 0, 128, SWIZZLE_NONE));
           tc_commit_pair_mc(bar_sfready + 8 * s, 1);
+          if (++s == static_cast<uint32_t>(STAGES)) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       tc_commit_pair_mc(bar_final + 8, 1);
@@ -388,11 +399,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint8_t* gSFA = smem + C::OFF_SFA + lane * 16;
     const uint8_t* gSFB = smem + C::OFF_SFB + lane * 16;
-    uint32_t it = 0;
+    uint32_t s = 0, ph = 0;
     for (int tile = unit; tile < num_tiles; tile += nunits) {
       bool ok = true;
-      for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
         if (!warp_wait(bar_full + 8 * s, ph, abort_flag)) {
           if (lane == 0) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
@@ -412,6 +422,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_sfready + 8 * s);
+        if (++s == static_cast<uint32_t>(STAGES)) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (!ok) break;
     }
