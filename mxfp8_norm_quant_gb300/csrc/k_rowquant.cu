@@ -155,15 +155,37 @@ cudaError_t launch_unswizzle_scales(const uint8_t* in, uint8_t* out, int rows, i
   return cudaLaunchKernelEx(&la.cfg, k_unswizzle_scales, in, out, rows, C);
 }
 
-cudaError_t launch_quant(const void* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
-                         unsigned int* /*fault*/, cudaStream_t stream) {
+namespace {
+
+template <int G>
+cudaError_t launch_quant_g(const uint16_t* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
+                           cudaStream_t stream) {
   const int nchunk = (cols + 255) / 256;
-  const long long tasks = static_cast<long long>(rows) * ((nchunk + 7) / 8) + 127;
+  const long long tasks = static_cast<long long>(rows) * ((nchunk + G - 1) / G) + 127;
   long long grid = 2LL * num_sms;
   const long long need = (tasks + ROW_WARPS - 1) / ROW_WARPS;
   if (grid > need) grid = need;
   LaunchAttrs la(dim3(static_cast<unsigned>(grid)), dim3(ROW_THREADS), 0, stream);
-  return cudaLaunchKernelEx(&la.cfg, k_quant<8>, static_cast<const uint16_t*>(x), q, sc, rows, cols);
+  return cudaLaunchKernelEx(&la.cfg, k_quant<G>, x, q, sc, rows, cols);
+}
+
+}  // namespace
+
+// Chunks per warp task: long tasks (8 chunks, 8 loads in flight per lane)
+// when there are rows to spare, shorter ones when that would leave warps
+// idle.  Measured on GB300 (CUDA-graph timing): 1024 x 2048: 2.3 us with 2
+// chunks per task vs 3.5 us with 8; 1024 x 3072: 3.3 us with 4 vs 3.8;
+// 4096 x 3072: 8.3 us with 4 vs 9.2.
+cudaError_t launch_quant(const void* xv, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
+                         unsigned int* /*fault*/, cudaStream_t stream) {
+  const uint16_t* x = static_cast<const uint16_t*>(xv);
+  const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
+  const long long nchunk = (cols + 255) / 256;
+  const auto tasks = [&](long long g) { return static_cast<long long>(rows) * ((nchunk + g - 1) / g); };
+  if (tasks(8) >= 4 * warps) return launch_quant_g<8>(x, q, sc, rows, cols, num_sms, stream);
+  if (tasks(4) * 5 >= warps * 4) return launch_quant_g<4>(x, q, sc, rows, cols, num_sms, stream);
+  if (tasks(2) * 5 >= warps * 4) return launch_quant_g<2>(x, q, sc, rows, cols, num_sms, stream);
+  return launch_quant_g<1>(x, q, sc, rows, cols, num_sms, stream);
 }
 
 // ---------------------------------------------------------------- probe
