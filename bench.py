@@ -393,51 +393,88 @@ def run_gpu(args, rank, world):
 
 
 def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
-    """Same metric end to end: pinned host inputs -> device, the step, outputs -> host."""
+    """Same metric end to end: every step copies its inputs from pinned host
+    memory to the device, runs the step through the C ABI and copies all of
+    its outputs (codes, scales, C) back to pinned host memory.  Steps are
+    pipelined as a serving loop runs them: copy-in, compute and copy-out on
+    three streams with double-buffered device and host buffers, so step i's
+    compute overlaps step i+1's copy-in and step i-1's copy-out.  The timed
+    region runs from before the first copy-in to after the last copy-out."""
     M = wl.m
     x_pin = x_h.pin_memory()
     a_pin = {k: a_h[k].pin_memory() for k in ks}
-    xd = torch.empty_like(x_pin, device=dev)
-    ad = {k: torch.empty_like(a_pin[k], device=dev) for k in ks}
-    q = torch.empty((M, H), dtype=torch.uint8, device=dev)
-    s = torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)
-    aq = {k: torch.empty((M, k), dtype=torch.uint8, device=dev) for k in ks}
-    as_ = {k: torch.empty(mx.mx_scale_bytes(M, k), dtype=torch.uint8, device=dev) for k in ks}
-    c = {k: torch.empty((M, N_OUT), dtype=torch.bfloat16, device=dev) for k in ks}
-    q_h = torch.empty_like(q, device="cpu").pin_memory()
-    s_h = torch.empty_like(s, device="cpu").pin_memory()
-    c_h = {k: torch.empty_like(c[k], device="cpu").pin_memory() for k in ks}
+
+    def buffers():
+        b = {"x": torch.empty_like(x_pin, device=dev),
+             "q": torch.empty((M, H), dtype=torch.uint8, device=dev),
+             "s": torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)}
+        for k in ks:
+            b[f"a{k}"] = torch.empty_like(a_pin[k], device=dev)
+            b[f"aq{k}"] = torch.empty((M, k), dtype=torch.uint8, device=dev)
+            b[f"as{k}"] = torch.empty(mx.mx_scale_bytes(M, k), dtype=torch.uint8, device=dev)
+            b[f"c{k}"] = torch.empty((M, N_OUT), dtype=torch.bfloat16, device=dev)
+        b["q_h"] = torch.empty_like(b["q"], device="cpu").pin_memory()
+        b["s_h"] = torch.empty_like(b["s"], device="cpu").pin_memory()
+        for k in ks:
+            b[f"c{k}_h"] = torch.empty_like(b[f"c{k}"], device="cpu").pin_memory()
+        return b
+
+    bufs = [buffers(), buffers()]
     h2d = x_pin.numel() * 2 + sum(a_pin[k].numel() * 2 for k in ks)
-    d2h = q.numel() + s.numel() + sum(c[k].numel() * 2 for k in ks)
-    sptr = stream.cuda_stream
+    d2h = bufs[0]["q"].numel() + bufs[0]["s"].numel() + sum(bufs[0][f"c{k}"].numel() * 2 for k in ks)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_comp = stream
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    for e in in_done + comp_done + out_done:
+        e.record(s_comp)
 
-    def step():
-        xd.copy_(x_pin, non_blocking=True)
-        mx.mx_rmsnorm_quant(xd, w_dev, EPS, q, s, M, H, sptr)
+    def step(i):
+        b = bufs[i % 2]
+        j = i % 2
+        # copy-in: buffer j's inputs were last read by the compute of step i-2
+        s_in.wait_event(comp_done[j])
+        with torch.cuda.stream(s_in):
+            b["x"].copy_(x_pin, non_blocking=True)
+            for k in ks:
+                b[f"a{k}"].copy_(a_pin[k], non_blocking=True)
+        in_done[j].record(s_in)
+        # compute: its outputs were last read by the copy-out of step i-2
+        s_comp.wait_event(in_done[j])
+        s_comp.wait_event(out_done[j])
+        sp = s_comp.cuda_stream
+        mx.mx_rmsnorm_quant(b["x"], w_dev, EPS, b["q"], b["s"], M, H, sp)
         for k in ks:
-            ad[k].copy_(a_pin[k], non_blocking=True)
-            mx.mx_quant_weights(ad[k], aq[k], as_[k], M, k, sptr)
-            mx.mx_gemm(aq[k], as_[k], wq[k][0], wq[k][1], c[k], M, N_OUT, k, sptr)
-        q_h.copy_(q, non_blocking=True)
-        s_h.copy_(s, non_blocking=True)
-        for k in ks:
-            c_h[k].copy_(c[k], non_blocking=True)
+            mx.mx_quant_weights(b[f"a{k}"], b[f"aq{k}"], b[f"as{k}"], M, k, sp)
+            mx.mx_gemm(b[f"aq{k}"], b[f"as{k}"], wq[k][0], wq[k][1], b[f"c{k}"], M, N_OUT, k, sp)
+        comp_done[j].record(s_comp)
+        # copy-out
+        s_out.wait_event(comp_done[j])
+        with torch.cuda.stream(s_out):
+            b["q_h"].copy_(b["q"], non_blocking=True)
+            b["s_h"].copy_(b["s"], non_blocking=True)
+            for k in ks:
+                b[f"c{k}_h"].copy_(b[f"c{k}"], non_blocking=True)
+        out_done[j].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        stream.synchronize()
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(args.steps):
+        step(i)
+    s_out.wait_event(comp_done[(args.steps - 1) % 2])
+    e1.record(s_out)
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     flops = sum(gemm_flops(M, N_OUT, k) for k in ks)
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "copy-in, compute and copy-out streams, double-buffered device and pinned host buffers"}
 
 
 # ------------------------------------------------------------------ CPU oracle arm
