@@ -48,6 +48,26 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ------------------------------------------------------------------ measured DRAM traffic
+
+def gemm_traffic_per_step(workload):
+    """DRAM bytes (read + write) of the step's GEMM launches from the ncu
+    capture committed under profiles/, or None when that capture is of
+    another workload or of an earlier version of the kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "k_gemm_mxf8_m1024_traffic.json")
+    try:
+        rec = json.load(open(path))["k_gemm_mxf8"]
+        h = hashlib.sha256()
+        for f in rec["source_files"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+    except (OSError, KeyError, ValueError):
+        return None
+    if h.hexdigest() != rec["source_sha256"] or workload != "m1024":
+        return None
+    return rec["dram_bytes_per_step"]
+
+
 # ------------------------------------------------------------------ traffic model
 
 def norm_quant_bytes(m, h=H):
@@ -373,7 +393,7 @@ def run_gpu(args, rank, world):
         "norm_quant_gbs": nq_gbs,
         "kernels": kern,
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp8_peak, "traffic": None,
+                     "frac": gemm_tflops / fp8_peak, "traffic": gemm_traffic_per_step(args.workload),
                      "kernel": "k_gemm_mxf8 (both launches of the step)",
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_PER_BF16} "
                                     "(nominal dense FP8/BF16 ratio)"},
