@@ -149,6 +149,15 @@ __device__ __forceinline__ int rows_walked(int M) {
   return FORM == OUT_MX_SWIZZLED ? ((M + 127) / 128) * 128 : M;
 }
 
+// (1 + w) lives in shared memory lane-interleaved: the 8 gains of lane l in
+// chunk c are two float4 at ((2c + h) * 32 + l) * 4, h = 0, 1, so a warp's
+// float4 load of them is one contiguous 512-byte run (element-order storage
+// puts lanes 32 bytes apart and costs twice the shared-memory wavefronts).
+__device__ __forceinline__ int gain_index(int i) {
+  const int c = i >> 8, l = (i >> 3) & 31, e = i & 7;
+  return ((2 * c + (e >> 2)) * 32 + l) * 4 + (e & 3);
+}
+
 // --------------------------------------------------------------- fused norm
 
 // CTA shape for WPR warps per row: as many whole row groups as fit in 16 warps.
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
   pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < nchunk * 256; i += THREADS)
-    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
+    g_s[gain_index(i)] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
   __syncthreads();
 
   int it = 0;
@@ -257,8 +266,8 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
       const int c = c0 + j;
       if (c >= nchunk) break;  // warp-uniform
       const int col = c * 256 + lane * 8;
-      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
-      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
+      const float4 ga = *reinterpret_cast<const float4*>(g_s + ((2 * (col >> 8)) * 32 + lane) * 4);
+      const float4 gb = *reinterpret_cast<const float4*>(g_s + ((2 * (col >> 8) + 1) * 32 + lane) * 4);
       const uint4 v = xv[j];
       const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
       const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
-    g_s[i] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
+    g_s[gain_index(i)] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
   __syncthreads();
 
   const int stride = gridDim.x * ROW_WARPS;
@@ -370,8 +379,8 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
     for (int j = 0; j < NCH; ++j) {
       if (j >= nchunk) break;  // warp-uniform
       const int col = j * 256 + lane * 8;
-      const float4 ga = *reinterpret_cast<const float4*>(g_s + col);
-      const float4 gb = *reinterpret_cast<const float4*>(g_s + col + 4);
+      const float4 ga = *reinterpret_cast<const float4*>(g_s + ((2 * (col >> 8)) * 32 + lane) * 4);
+      const float4 gb = *reinterpret_cast<const float4*>(g_s + ((2 * (col >> 8) + 1) * 32 + lane) * 4);
       const uint4 v = xv[j];
       const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr2), make_float2(ga.x, ga.y));
       const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
