@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
       const int c = c0 + j;
       if (c >= nchunk) break;  // warp-uniform
       const uint4 v = xv[j];
-      quantize_store<false>(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
+      quantize_store<false, false>(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
                      make_float2(bf16lo(v.z), bf16hi(v.z)), make_float2(bf16lo(v.w), bf16hi(v.w)),
                      c * 256 + lane * 8 < cols, lane, row, c, cols, words, q, sc);
     }

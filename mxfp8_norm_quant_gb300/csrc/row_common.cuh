@@ -29,7 +29,7 @@
 //     through shared memory;
 //   * 4 lanes hold one 32-element MX block: amax by two shuffles, the UE8M0
 //     byte from the exponent field, one cvt per element pair, an 8-byte
-//     store of codes per lane and one 4-byte store per 4 scales.
+//     store of codes per lane and a byte store of the scale.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -91,7 +91,7 @@ __device__ __forceinline__ float warp_tree(float p) {
 // their codes and the scales of the 256-element chunk c of row `row`:
 // swizzled, lanes 0 and 16 store the chunk's two 4-scale words; row-major,
 // the first lane of each block stores its byte.
-template <bool ROWMAJOR>
+template <bool ROWMAJOR, bool SCALE_BYTES>
 __device__ __forceinline__ void quantize_store(float2 y01, float2 y23, float2 y45, float2 y67, bool valid,
                                                int lane, int row, int c, int H, int words, uint8_t* __restrict__ q,
                                                uint8_t* __restrict__ sc) {
@@ -111,8 +111,15 @@ __device__ __forceinline__ void quantize_store(float2 y01, float2 y23, float2 y4
   if (valid) *reinterpret_cast<uint2*>(q + static_cast<size_t>(row) * H + col) = codes;
   if constexpr (ROWMAJOR) {
     if (valid && (lane & 3) == 0) sc[static_cast<size_t>(row) * (H >> 5) + (col >> 5)] = static_cast<uint8_t>(byte);
+  } else if constexpr (SCALE_BYTES) {
+    // the first lane of each block stores its byte at its F8_128x4 place;
+    // a block past the row's end inside the last 4-column group is padding (0)
+    const int wd = 2 * c + (lane >> 4);
+    if ((lane & 3) == 0 && wd < words)
+      sc[scale_word_off(row, wd, words) + ((lane >> 2) & 3)] = valid ? static_cast<uint8_t>(byte) : uint8_t{0};
   } else {
-    // the four scale bytes of each 128-element word: block b = lane / 4
+    // the four scale bytes of each 128-element word gathered by two shuffles,
+    // one 4-byte store (block b = lane / 4)
     uint32_t wv = valid ? byte << (8 * ((lane >> 2) & 3)) : 0u;
     wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
     wv |= __shfl_xor_sync(0xffffffffu, wv, 8);
@@ -128,7 +135,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Writes the 8 normalised values a lane holds in the kernel's output form.
 // For OUT_BF16, `q` is the [M][H] bf16 output and `sc` is unused.
-template <int FORM>
+template <int FORM, bool SCALE_BYTES = true>
 __device__ __forceinline__ void emit(float2 y01, float2 y23, float2 y45, float2 y67, bool valid, int lane, int row,
                                      int c, int H, int words, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
   if constexpr (FORM == OUT_BF16) {
@@ -138,7 +145,7 @@ __device__ __forceinline__ void emit(float2 y01, float2 y23, float2 y45, float2 
       *reinterpret_cast<uint4*>(q + (static_cast<size_t>(row) * H + c * 256 + lane * 8) * 2) = v;
     }
   } else {
-    quantize_store<FORM == OUT_MX_ROWMAJOR>(y01, y23, y45, y67, valid, lane, row, c, H, words, q, sc);
+    quantize_store<FORM == OUT_MX_ROWMAJOR, SCALE_BYTES>(y01, y23, y45, y67, valid, lane, row, c, H, words, q, sc);
   }
 }
 
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
 // registers, a TMA bulk copy brings its next row into the slot, so memory
 // and arithmetic overlap within the warp (the register-only kernel above
 // loads, then computes, then loads again).  NCH * 256 >= H.
-template <int NCH, int FORM>
+template <int NCH, int FORM, bool SCALE_BYTES>
 __global__ void __launch_bounds__(ROW_THREADS, 1)
     k_rmsnorm_quant_pf(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
                        uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, unsigned int* fault) {
@@ -386,16 +393,24 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
       const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr2), make_float2(ga.z, ga.w));
       const float2 y45 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr2), make_float2(gb.x, gb.y));
       const float2 y67 = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr2), make_float2(gb.z, gb.w));
-      emit<FORM>(y01, y23, y45, y67, col < H, lane, row, j, H, words, q, sc);
+      emit<FORM, SCALE_BYTES>(y01, y23, y45, y67, col < H, lane, row, j, H, words, q, sc);
       asm volatile("" ::: "memory");
     }
   }
 }
 
+// Scale stores of the swizzled form: a byte per block from the block's first
+// lane is fewer instructions and measured faster for up to ~10k rows; beyond,
+// where the launch is bandwidth-bound, one 4-byte store per 4 blocks is
+// (same-box timing at H = 6144, bytes vs words: 1024 rows 6.4 vs 6.9 us, 8192
+// rows 31.9 vs 33.3 us, 16384 rows 54.7 vs 53.4 us, 32768 rows 109.7 vs 102.5).
+constexpr int SCALE_BYTE_STORES_MAX_ROWS = 12288;
+
 template <int NCH, int FORM>
 cudaError_t launch_norm_pf(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                            int num_sms, unsigned int* fault, cudaStream_t stream) {
-  auto kern = k_rmsnorm_quant_pf<NCH, FORM>;
+  auto kern = M <= SCALE_BYTE_STORES_MAX_ROWS ? k_rmsnorm_quant_pf<NCH, FORM, true>
+                                              : k_rmsnorm_quant_pf<NCH, FORM, FORM != OUT_MX_SWIZZLED>;
   const int nchunk = (H + 255) / 256;
   const int smem = nchunk * 1024 + ROW_WARPS * nchunk * 512 + ROW_WARPS * 8;
   cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
