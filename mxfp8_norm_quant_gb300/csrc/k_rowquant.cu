@@ -11,8 +11,10 @@ namespace {
 
 // --------------------------------------------------------------- plain quant
 
-// A warp task is up to G consecutive chunks of one row.
-template <int G>
+// A warp task is up to G consecutive chunks of one row.  SCALE_BYTES: each
+// block's first lane stores its scale byte (as the norm kernels do while the
+// launch is latency-bound) instead of one 4-byte store per 4 blocks.
+template <int G, bool SCALE_BYTES>
 __global__ void __launch_bounds__(ROW_THREADS, 2)
     k_quant(const uint16_t* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int rows,
             int cols) {
@@ -48,7 +50,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 2)
       const int c = c0 + j;
       if (c >= nchunk) break;  // warp-uniform
       const uint4 v = xv[j];
-      quantize_store<false, false>(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
+      quantize_store<false, SCALE_BYTES>(make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
                      make_float2(bf16lo(v.z), bf16hi(v.z)), make_float2(bf16lo(v.w), bf16hi(v.w)),
                      c * 256 + lane * 8 < cols, lane, row, c, cols, words, q, sc);
     }
@@ -160,13 +162,14 @@ namespace {
 template <int G>
 cudaError_t launch_quant_g(const uint16_t* x, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
                            cudaStream_t stream) {
+  auto kern = rows <= SCALE_BYTE_STORES_MAX_ROWS ? k_quant<G, true> : k_quant<G, false>;
   const int nchunk = (cols + 255) / 256;
   const long long tasks = static_cast<long long>(rows) * ((nchunk + G - 1) / G) + 127;
   long long grid = 2LL * num_sms;
   const long long need = (tasks + ROW_WARPS - 1) / ROW_WARPS;
   if (grid > need) grid = need;
   LaunchAttrs la(dim3(static_cast<unsigned>(grid)), dim3(ROW_THREADS), 0, stream);
-  return cudaLaunchKernelEx(&la.cfg, k_quant<G>, x, q, sc, rows, cols);
+  return cudaLaunchKernelEx(&la.cfg, kern, x, q, sc, rows, cols);
 }
 
 }  // namespace
