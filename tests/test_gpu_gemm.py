@@ -76,7 +76,7 @@ def test_small_integers_exact(cuda_dev, tile):
 
 
 SHAPES = [(128, 6144, 2048), (1, 96, 32), (300, 416, 288), (129, 256, 4096), (512, 1024, 3072), (77, 6144, 160),
-          (1000, 2016, 1024)]
+          (1000, 2016, 1024), (300, 512, 16384)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
