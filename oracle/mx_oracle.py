@@ -21,7 +21,7 @@ no formula:
 * an MXFP8 GEMM with N=6144, K=2048 (o_proj) and K=3072 (down_proj), BF16 out
   (PR #64659, GEMM-RS microbenchmark table).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 R1  Gemma RMSNorm: y = x * rsqrt(mean(x^2) + eps) * (1 + w), mean over the
     whole row, eps inside the square root.
