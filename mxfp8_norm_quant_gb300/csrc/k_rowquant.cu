@@ -176,9 +176,9 @@ cudaError_t launch_quant_g(const uint16_t* x, uint8_t* q, uint8_t* sc, int rows,
 
 // Chunks per warp task: long tasks (8 chunks, 8 loads in flight per lane)
 // when there are rows to spare, shorter ones when that would leave warps
-// idle.  Measured on GB300 (CUDA-graph timing): 1024 x 2048: 2.3 us with 2
-// chunks per task vs 3.5 us with 8; 1024 x 3072: 3.3 us with 4 vs 3.8;
-// 4096 x 3072: 8.3 us with 4 vs 9.2.
+// idle.  Measured on GB300 (CUDA-graph timing, inputs rotating beyond L2):
+// 1024 x 2048: 2.9 / 3.0 / 3.9 us with 2 / 4 / 8 chunks per task;
+// 1024 x 3072: 3.9 us with 4 vs 4.4 with 8; 4096 x 3072: 8.8 us with 4 vs 9.1.
 cudaError_t launch_quant(const void* xv, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
                          unsigned int* /*fault*/, cudaStream_t stream) {
   const uint16_t* x = static_cast<const uint16_t*>(xv);

@@ -454,9 +454,10 @@ cudaError_t dispatch_norm(const void* xv, const void* wv, float eps, uint8_t* q,
   }
   if (nchunk > 16 && nchunk <= 24) {
     // rows of 4097..6144 elements, at most one row per warp; measured on
-    // GB300 at H = 6144 (CUDA-graph timing): M = 512: 3 warps per row 5.2 us
-    // vs 6.8 us one; M = 768: 6 warps per row 6.75 us vs 7.7; M >= 896: the
-    // prefetching kernel (M = 1024: 7.8 us vs 8.5 us for one warp per row)
+    // GB300 at H = 6144 (CUDA-graph timing, inputs rotating beyond L2):
+    // M = 128: 6 warps per row 3.8 us vs 6.1 one; M = 512: 3 warps per row
+    // 5.8 us vs 7.2 one; M = 768: all variants 8.3-8.4 us; M >= 896: the
+    // prefetching kernel (M = 1024: 8.5 us vs 8.8 one, 9.1 three)
     if (M >= 896) return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
     if (M > 256 && M <= 640) return launch_norm<3, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
     return launch_norm<6, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
