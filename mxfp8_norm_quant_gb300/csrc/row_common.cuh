@@ -87,6 +87,57 @@ __device__ __forceinline__ float warp_tree(float p) {
   return p;
 }
 
+// The sum of squares of a row of NCH = 8, 16 or 24 chunks (lane l holds
+// elements [256c + 8l, +8) of chunk c), in the same pairwise tree as
+// warp_tree per chunk followed by the chunk-level tree, but with 36 instead
+// of 120 shuffles for NCH = 24: the three lane levels below 8 lanes are a
+// reduce-scatter (at each level a lane keeps half of its chunk partials and
+// adds its partner's half of the same chunks), so that lane l ends with the
+// 64-element sums of chunks c = l % 8 (mod 8); two butterfly levels finish
+// those chunks and three more combine chunks 8k .. 8k+7, whose lanes differ
+// in bits 0-2.  Every node is the same two children added, so the result is
+// bit-identical to the per-chunk butterflies.
+template <int NCH>
+__device__ __forceinline__ float row_square_tree_rs(const uint4 (&xv)[NCH], int lane) {
+  static_assert(NCH == 8 || NCH == 16 || NCH == 24, "chunk runs of 8, 16 or 24");
+  float v[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) v[c] = lane_square_tree(xv[c]);
+  const bool b0 = lane & 1, b1 = (lane >> 1) & 1, b2 = (lane >> 2) & 1;
+  float u1[NCH / 2];  // 16-element sums of chunks 2k + b0
+#pragma unroll
+  for (int k = 0; k < NCH / 2; ++k) {
+    const float keep = b0 ? v[2 * k + 1] : v[2 * k];
+    const float give = b0 ? v[2 * k] : v[2 * k + 1];
+    u1[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 1));
+  }
+  float u2[NCH / 4];  // 32-element sums of chunks 4k + 2 b1 + b0
+#pragma unroll
+  for (int k = 0; k < NCH / 4; ++k) {
+    const float keep = b1 ? u1[2 * k + 1] : u1[2 * k];
+    const float give = b1 ? u1[2 * k] : u1[2 * k + 1];
+    u2[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 2));
+  }
+  float u3[NCH / 8];  // 64-element sums of chunks 8k + (l & 7)
+#pragma unroll
+  for (int k = 0; k < NCH / 8; ++k) {
+    const float keep = b2 ? u2[2 * k + 1] : u2[2 * k];
+    const float give = b2 ? u2[2 * k] : u2[2 * k + 1];
+    u3[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+  }
+#pragma unroll
+  for (int k = 0; k < NCH / 8; ++k) {
+    u3[k] = __fadd_rn(u3[k], __shfl_xor_sync(0xffffffffu, u3[k], 8));   // 128 elements
+    u3[k] = __fadd_rn(u3[k], __shfl_xor_sync(0xffffffffu, u3[k], 16));  // the chunk
+    u3[k] = __fadd_rn(u3[k], __shfl_xor_sync(0xffffffffu, u3[k], 1));   // chunk pairs
+    u3[k] = __fadd_rn(u3[k], __shfl_xor_sync(0xffffffffu, u3[k], 2));
+    u3[k] = __fadd_rn(u3[k], __shfl_xor_sync(0xffffffffu, u3[k], 4));   // chunks 8k .. 8k+7
+  }
+  if constexpr (NCH == 8) return u3[0];
+  if constexpr (NCH == 16) return __fadd_rn(u3[0], u3[1]);
+  return __fadd_rn(__fadd_rn(u3[0], u3[1]), u3[2]);
+}
+
 // Quantises the 8 values a lane holds (4 lanes = one MX block) and stores
 // their codes and the scales of the 256-element chunk c of row `row`:
 // swizzled, lanes 0 and 16 store the chunk's two 4-scale words; row-major,
@@ -209,12 +260,23 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
 
   pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
   pdl_launch_dependents();
+  // the first row's loads go out before the gain set-up, whose latency they hide
+  const int row0 = blockIdx.x + gridDim.x * grp;
+  uint4 xv[NCH];
+  if (row0 < M) {
+    const uint16_t* xr = x + static_cast<size_t>(row0) * H;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int col = (c0 + j) * 256 + lane * 8;
+      xv[j] = col < H ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
+    }
+  }
   for (int i = threadIdx.x; i < nchunk * 256; i += THREADS)
     g_s[gain_index(i)] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
   __syncthreads();
 
   int it = 0;
-  for (int row = blockIdx.x + gridDim.x * grp; row < Mw; row += gridDim.x * GROUPS, ++it) {
+  for (int row = row0; row < Mw; row += gridDim.x * GROUPS, ++it) {
     if (row >= M) {
       // padding row of the last 128-row block: its scale bytes are zero
       if (wi == 0)
@@ -222,12 +284,13 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
           *reinterpret_cast<uint32_t*>(sc + scale_word_off(row, wd, words)) = 0u;
       continue;
     }
-    const uint16_t* xr = x + static_cast<size_t>(row) * H;
-    uint4 xv[NCH];
+    if (row != row0) {
+      const uint16_t* xr = x + static_cast<size_t>(row) * H;
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int col = (c0 + j) * 256 + lane * 8;
-      xv[j] = col < H ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < NCH; ++j) {
+        const int col = (c0 + j) * 256 + lane * 8;
+        xv[j] = col < H ? ldg_stream(xr + col) : make_uint4(0, 0, 0, 0);
+      }
     }
 
     // pass 1: sum of squares, pairwise tree over the warp's chunks
@@ -292,8 +355,10 @@ __global__ void __launch_bounds__(NormCta<WPR>::THREADS, 1)
 // shared-memory slot of one row; while it computes the row it holds in
 // registers, a TMA bulk copy brings its next row into the slot, so memory
 // and arithmetic overlap within the warp (the register-only kernel above
-// loads, then computes, then loads again).  NCH * 256 >= H.
-template <int NCH, int FORM, bool SCALE_BYTES>
+// loads, then computes, then loads again).  NCH * 256 >= H.  RS selects
+// the reduce-scatter form of the sum of squares (same result, fewer
+// shuffles; measured faster for launches of 1-4 rows per warp only).
+template <int NCH, int FORM, bool SCALE_BYTES, bool RS>
 __global__ void __launch_bounds__(ROW_THREADS, 1)
     k_rmsnorm_quant_pf(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, float eps,
                        uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, unsigned int* fault) {
@@ -315,16 +380,31 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   fence_barrier_init();
   pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
   pdl_launch_dependents();
-  for (int i = threadIdx.x; i < nchunk * 256; i += ROW_THREADS)
-    g_s[gain_index(i)] = i < H ? __fadd_rn(1.0f, __uint_as_float(static_cast<uint32_t>(w[i]) << 16)) : 0.0f;
-  __syncthreads();
-
+  // Order of the first requests: this thread's gains, then the warp's first
+  // row, then the gain table.  The gains go out ahead of the burst of row
+  // copies (issued after them they queue behind it and hold every warp at
+  // the barrier below), and the first row's copy ahead of the table's
+  // set-up, whose latency it hides.
+  constexpr int GAINS_PER_THREAD = (NCH * 256 + ROW_THREADS - 1) / ROW_THREADS;
+  uint32_t wr[GAINS_PER_THREAD];
+#pragma unroll
+  for (int k = 0; k < GAINS_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    wr[k] = i < H ? static_cast<uint32_t>(w[i]) : 0u;
+  }
   const int stride = gridDim.x * ROW_WARPS;
   int row = blockIdx.x + gridDim.x * warp;
+  __syncwarp();  // the barrier is initialised before its copy is issued
   if (lane == 0 && row < M) {
     mbar_arrive_expect_tx(bar, row_bytes);
     bulk_g2s(slot_s, x + static_cast<size_t>(row) * H, row_bytes, bar);
   }
+#pragma unroll
+  for (int k = 0; k < GAINS_PER_THREAD; ++k) {
+    const int i = threadIdx.x + k * ROW_THREADS;
+    if (i < nchunk * 256) g_s[gain_index(i)] = i < H ? __fadd_rn(1.0f, __uint_as_float(wr[k] << 16)) : 0.0f;
+  }
+  __syncthreads();
   uint32_t phase = 0;
   for (; row < Mw; row += stride) {
     if (row >= M) {
@@ -345,26 +425,31 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
       xv[j] = col < H ? *reinterpret_cast<const uint4*>(slot + j * 512 + lane * 16) : make_uint4(0, 0, 0, 0);
     }
 
-    // pass 1: sum of squares, pairwise tree over the row's chunks
-    float lvl[6];
+    float ss;
+    if constexpr (RS) {
+      ss = row_square_tree_rs<NCH>(xv, lane);
+    } else {
+      // pass 1: sum of squares, pairwise tree over the row's chunks
+      float lvl[6];
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      float t = warp_tree(lane_square_tree(xv[j]));
-      int k = 0;
+      for (int j = 0; j < NCH; ++j) {
+        float t = warp_tree(lane_square_tree(xv[j]));
+        int k = 0;
 #pragma unroll
-      for (; k < 6; ++k) {
-        if (((j >> k) & 1) == 0) break;
-        t = __fadd_rn(lvl[k], t);
+        for (; k < 6; ++k) {
+          if (((j >> k) & 1) == 0) break;
+          t = __fadd_rn(lvl[k], t);
+        }
+        lvl[k] = t;
       }
-      lvl[k] = t;
-    }
-    float ss = 0.0f;
-    bool first = true;
+      ss = 0.0f;
+      bool first = true;
 #pragma unroll
-    for (int k = 0; k < 6; ++k) {
-      if ((NCH >> k) & 1) {
-        ss = first ? lvl[k] : __fadd_rn(lvl[k], ss);
-        first = false;
+      for (int k = 0; k < 6; ++k) {
+        if ((NCH >> k) & 1) {
+          ss = first ? lvl[k] : __fadd_rn(lvl[k], ss);
+          first = false;
+        }
       }
     }
     // every lane's reads of the slot are consumed: the slot may take the next row
@@ -406,11 +491,23 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
 // rows 31.9 vs 33.3 us, 16384 rows 54.7 vs 53.4 us, 32768 rows 109.7 vs 102.5).
 constexpr int SCALE_BYTE_STORES_MAX_ROWS = 12288;
 
+// The reduce-scatter sum of squares (bit-identical) is faster while a
+// launch gives each warp 1-4 rows and slower with more (same-box timing at
+// H = 6144, per-chunk butterflies vs reduce-scatter: 1024 rows 7.9 vs 8.05 us,
+// 2048 rows 11.8 vs 11.3, 4096 rows 19.1 vs 18.3, 8192 rows 31.4 vs 31.0,
+// 32768 rows 97.5 vs 107.7); measured for rows of 17-24 chunks only.
+template <int NCH>
+bool norm_pf_uses_rs(int M, int num_sms) {
+  const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
+  return NCH == 24 && 2LL * M > warps && M <= 4 * warps;
+}
+
 template <int NCH, int FORM>
 cudaError_t launch_norm_pf(const uint16_t* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                            int num_sms, unsigned int* fault, cudaStream_t stream) {
-  auto kern = M <= SCALE_BYTE_STORES_MAX_ROWS ? k_rmsnorm_quant_pf<NCH, FORM, true>
-                                              : k_rmsnorm_quant_pf<NCH, FORM, FORM != OUT_MX_SWIZZLED>;
+  auto kern = norm_pf_uses_rs<NCH>(M, num_sms) ? k_rmsnorm_quant_pf<NCH, FORM, true, NCH == 24>
+              : M <= SCALE_BYTE_STORES_MAX_ROWS ? k_rmsnorm_quant_pf<NCH, FORM, true, false>
+                                                : k_rmsnorm_quant_pf<NCH, FORM, FORM != OUT_MX_SWIZZLED, false>;
   const int nchunk = (H + 255) / 256;
   const int smem = nchunk * 1024 + ROW_WARPS * nchunk * 512 + ROW_WARPS * 8;
   cudaError_t err = set_smem_once(reinterpret_cast<const void*>(kern), smem);
