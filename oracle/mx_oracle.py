@@ -201,8 +201,9 @@ def gemma_rmsnorm_f32(x_bits: np.ndarray, w_bits: np.ndarray, eps: float) -> np.
     xf = bf16_bits_to_f32(x_bits)
     wf = bf16_bits_to_f32(w_bits)
     h = xf.shape[1]
-    sq = xf * xf                                   # fp32 products
-    ss = pairwise_sum_f32(sq)                      # (M,)
+    with np.errstate(over="ignore"):               # a square past the fp32 range is +inf, as on the GPU
+        sq = xf * xf                               # fp32 products
+        ss = pairwise_sum_f32(sq)                  # (M,)
     ms = ss / np.float32(h)                        # mean
     v = ms + np.float32(eps)
     s = np.sqrt(v)                                 # correctly rounded fp32 sqrt
