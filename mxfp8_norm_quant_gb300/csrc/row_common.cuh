@@ -550,13 +550,22 @@ cudaError_t dispatch_norm(const void* xv, const void* wv, float eps, uint8_t* q,
     return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
   }
   if (nchunk > 16 && nchunk <= 24) {
-    // rows of 4097..6144 elements, at most one row per warp; measured on
-    // GB300 at H = 6144 (CUDA-graph timing, inputs rotating beyond L2):
-    // M = 128: 6 warps per row 3.8 us vs 6.1 one; M = 512: 3 warps per row
-    // 5.8 us vs 7.2 one; M = 768: all variants 8.3-8.4 us; M >= 896: the
-    // prefetching kernel (M = 1024: 8.5 us vs 8.8 one, 9.1 three)
+    // rows of 4097..6144 elements, at most one row per warp.  A register
+    // kernel is best while its rows fit one round (6 warps per row: 2 rows
+    // per CTA; 3 warps: 5 rows per CTA); past that the prefetching kernel.
+    // Measured on GB300 at H = 6144 (CUDA-graph timing, inputs rotating
+    // beyond L2; swizzled / row-major / bf16 forms, us):
+    //   M = 128: 6 warps per row 3.3 / 3.1 / 2.9, prefetching 5.5 / 6.1 / 4.4;
+    //   M = 704: 3 warps per row 6.3 / 6.0 / 5.9, 6 warps 7.8 / 7.5 / 7.3,
+    //            prefetching 6.9 / 7.6 / 6.2;
+    //   M = 768: 3 warps (two rounds) 8.3 / 7.9 / 7.3, 6 warps 7.9 / 7.5 / 7.4,
+    //            prefetching 7.2 / 7.9 / 6.3;
+    //   M = 1024: prefetching 7.8 / 8.4 / 7.0.
     if (M >= 896) return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (M > 256 && M <= 640) return launch_norm<3, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
+    if (M > 256 && M <= NormCta<3>::GROUPS * num_sms)
+      return launch_norm<3, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
+    if (M > 256 && FORM != OUT_MX_ROWMAJOR)
+      return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
     return launch_norm<6, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
   }
   if (nchunk <= 24 && (M >= 512 || rows_per_warp > 0)) {

@@ -53,6 +53,22 @@ def test_norm_quant_small(cuda_dev, M, H):
     _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
 
 
+# Row counts at H = 6144 on either side of each kernel choice of the
+# dispatcher on a 152-SM GPU: 6 warps per row (<= 256 rows), 3 warps per row
+# (<= 760), the prefetching kernel (>= 761; the row-major form keeps 6 warps
+# per row below 896), and its reduce-scatter sum of squares (1217-9728 rows).
+# Every variant must give the same bytes.
+DISPATCH_ROWS = [256, 257, 760, 761, 895, 896, 1216, 1217, 9728, 9729]
+
+
+@pytest.mark.parametrize("M", DISPATCH_ROWS)
+def test_norm_quant_dispatch_boundaries(cuda_dev, M):
+    H = 6144
+    x, w = W.norm_inputs(M, H, seed=M + 11)
+    rq, rs = O.rmsnorm_quant(bf16_bits(x), bf16_bits(w), 1e-6)
+    _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
+
+
 @pytest.mark.parametrize("M,H", SMALL)
 def test_quant_small(cuda_dev, M, H):
     x = W.normal_bf16((M, H), 1.0, seed=M + H, tag="A")

@@ -16,10 +16,12 @@ from mxtest import bf16_bits, np_u8
 pytestmark = pytest.mark.gpu
 
 # row counts that reach every row-ownership path of the dispatcher (rows
-# split over warps, one warp per row, the prefetching kernel) with ragged
-# 128-row blocks; widths with 1, 5 and 192 scale columns per row
-SHAPES = [(1, 6144), (300, 6144), (1024, 6144), (5000, 6144), (77, 160), (640, 2048), (3000, 4096),
-          (2500, 32), (9, 16384)]
+# split over 6 or 3 warps, one warp per row, the prefetching kernel; 720 and
+# 800 rows sit on either side of the 3-warp kernel's one-round limit on a
+# 152-SM GPU) with ragged 128-row blocks; widths with 1, 5 and 192 scale
+# columns per row
+SHAPES = [(1, 6144), (300, 6144), (720, 6144), (800, 6144), (1024, 6144), (5000, 6144), (77, 160), (640, 2048),
+          (3000, 4096), (2500, 32), (9, 16384)]
 
 
 def _ids(shapes):
