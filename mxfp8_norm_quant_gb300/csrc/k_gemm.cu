@@ -33,7 +33,9 @@
 //              and stored as 32 E4M3 codes and one UE8M0 byte at its F8_128x4
 //              place, so C leaves the kernel as an MXFP8 operand for the next
 //              GEMM (the quantised-activation output of vLLM PR #64659,
-//              Details / "GEMM-RS with a quantized input").
+//              Details / "GEMM-RS with a quantized input").  When a CTA has
+//              more than one tile, warps 6-9 (idle by then) drain the second
+//              half of the columns of its last tile.
 // The single threads that issue copies, scale moves and MMAs are
 // instruction-bound, so their loops keep descriptors as 32-bit words and ring
 // positions as counters.  Two accumulators let the epilogue of one tile
