@@ -17,10 +17,12 @@
 //              (tensor maps, 128-byte swizzle) and the 512-byte F8_128x4 scale
 //              blocks of A (one) and B (two consecutive) into a ring of
 //              STAGES shared-memory stages;
-//   warps 6-9  scale warps, one per TMEM lane quarter: move a stage's scale
-//              blocks from shared memory into that stage's TMEM scale slot
-//              with tcgen05.st (keeping the tensor pipe free of scale copies,
-//              which cost it ~200 cycles each when issued as tcgen05.cp);
+//   warps 6-9  scales into TMEM: one CTA, four scale warps (one per TMEM lane
+//              quarter) move a stage's scale blocks from shared memory into
+//              its TMEM scale slot with tcgen05.st; a pair, one thread of the
+//              leader copies both CTAs' blocks with tcgen05.cp.cta_group::2
+//              and commits to the stage's sf_ready barrier.  Either way the
+//              MMA issuer does not issue the scale moves;
 //   warp 1     TMEM owner and (leader CTA) MMA issuer: once a stage's scales
 //              are in TMEM (in both CTAs of a pair), four
 //              tcgen05.mma.kind::mxf8f6f4.block_scale (K=32 each, scale byte
@@ -39,10 +41,10 @@
 // The single threads that issue copies, scale moves and MMAs are
 // instruction-bound, so their loops keep descriptors as 32-bit words and ring
 // positions as counters.  Two accumulators let the epilogue of one tile
-// overlap the main loop of the next.  Tiles are dealt round-robin, N-tile fastest, so concurrently running
-// CTAs share A rows and all of B in L2.  In a pair each CTA's copies complete
-// on its own barriers; both CTAs' scale warps report each stage to the
-// leader, and both CTAs' epilogues hand their accumulator back to it.
+// overlap the main loop of the next.  Tiles are dealt round-robin, N-tile
+// fastest, so concurrently running CTAs share A rows and all of B in L2.  In
+// a pair both CTAs' copies complete on the leader's barriers, and both CTAs'
+// epilogues hand their accumulator back to it.
 //
 // F8_128x4 and TMEM: the MMA reads row r's scales from TMEM column
 // (slot + r/32) of lane r%32 in the lane quarters, scale column c in byte c
