@@ -381,10 +381,10 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   pdl_wait();  // the previous kernel of the stream has finished with x, w, q and sc
   pdl_launch_dependents();
   // Order of the first requests: this thread's gains, then the warp's first
-  // row, then the gain table.  The gains go out ahead of the burst of row
-  // copies (issued after them they queue behind it and hold every warp at
-  // the barrier below), and the first row's copy ahead of the table's
-  // set-up, whose latency it hides.
+  // row, then the gain table.  The gain loads go out before the burst of
+  // row copies (issued after it, they queue behind it and hold every warp at
+  // the barrier below), and the first row's copy goes out before the
+  // table's set-up, whose latency it hides.
   constexpr int GAINS_PER_THREAD = (NCH * 256 + ROW_THREADS - 1) / ROW_THREADS;
   uint32_t wr[GAINS_PER_THREAD];
 #pragma unroll
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(ROW_THREADS, 1)
   }
   const int stride = gridDim.x * ROW_WARPS;
   int row = blockIdx.x + gridDim.x * warp;
-  __syncwarp();  // the barrier is initialised before its copy is issued
+  __syncwarp();
   if (lane == 0 && row < M) {
     mbar_arrive_expect_tx(bar, row_bytes);
     bulk_g2s(slot_s, x + static_cast<size_t>(row) * H, row_bytes, bar);
