@@ -187,6 +187,21 @@ mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s,
                         int64_t M, int64_t N, int64_t K,
                         int tile_m, int tile_n, mx_stream_t stream);
 
+/* Self-test of the GEMM's failure handling.  Launches mx_gemm_ex's kernel
+ * with its producer issuing no copies, so that every bounded wait in it runs
+ * out after wait_ns nanoseconds (100 us <= wait_ns <= 1 s, else
+ * MX_ERR_SHAPE; M >= 1).  The kernel then takes the path a real stall would:
+ * it sets bits in the device fault word (read them with mx_device_fault),
+ * frees its tensor memory and exits; no thread is left waiting.  out is not
+ * written.  Arguments are validated as for mx_gemm_ex and must describe real
+ * buffers of those sizes.  For tests only: it exercises the give-up path
+ * without a broken device. */
+mx_status mx_gemm_selftest_stall(const uint8_t* a_q, const uint8_t* a_s,
+                                 const uint8_t* b_q, const uint8_t* b_s,
+                                 void* out, int64_t M, int64_t N, int64_t K,
+                                 int tile_m, int tile_n, uint64_t wait_ns,
+                                 mx_stream_t stream);
+
 /* The launch configuration mx_gemm would use on the current device: output
  * tile, pipeline stages and grid size (CTAs).  Any out-pointer may be NULL. */
 mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m,
@@ -203,7 +218,11 @@ mx_status mx_e4m3_encode_f32(const float* in, uint8_t* out, int64_t n,
  * A kernel that gives up a bounded wait (about one second; only a bug or a
  * broken device can cause it) sets a bit here and exits cleanly instead of
  * hanging.  *code receives the bits (0 = no fault).  Synchronises the
- * current device.  Returns MX_ERR_DEVICE_TIMEOUT if a bit was set. */
+ * current device first (cudaDeviceSynchronize: kernels on every stream,
+ * blocking or not), so the word is read after every kernel launched before
+ * the call has finished.  Calls from several host threads, or launches
+ * racing this call, may see or clear each other's bits.  Returns
+ * MX_ERR_DEVICE_TIMEOUT if a bit was set. */
 mx_status mx_device_fault(uint32_t* code);
 
 /* The cudaError_t of the most recent failing CUDA call on this host thread. */

@@ -3,8 +3,13 @@
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI declared in include/mxgemm.h.  Functions named
 ``mx_*`` mirror the C entry points one to one; they accept torch tensors
-(their device pointers are passed) or raw integer device addresses.  The
-small helpers at the bottom only allocate outputs with torch and call them.
+(their device pointers are passed) or raw integer device addresses.  A torch
+tensor is checked before its address is passed: it must be a contiguous CUDA
+tensor on the current device holding at least the bytes the call reads or
+writes (a ValueError otherwise), so that a wrong buffer is caught on the host
+and never becomes an out-of-bounds access on the GPU.  Raw integer addresses
+are passed as given.  The small helpers at the bottom only allocate outputs
+with torch and call them.
 
 There is no fallback: if libmxgemm.so has not been built, every call raises.
 """
@@ -31,6 +36,7 @@ EXPORTED = (
     "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
     "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
+    "mx_gemm_selftest_stall",
 )
 
 # scale layouts of mx_rmsnorm_quant_ex
@@ -74,6 +80,7 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, vp]
     L.mx_gemm_ex.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, vp]
     L.mx_gemm_quant.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, i64, i64, i64, i32, i32, vp]
+    L.mx_gemm_selftest_stall.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, ctypes.c_uint64, vp]
     L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -83,7 +90,8 @@ def lib() -> ctypes.CDLL:
     L.mx_version.argtypes = []
     for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
                  "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
-                 "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version"):
+                 "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version",
+                 "mx_gemm_selftest_stall"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -114,6 +122,38 @@ def _check(fn: str, status: int):
         raise MxError(fn, status, lib().mx_last_cuda_error())
 
 
+def _scale_bytes_py(rows: int, cols: int) -> int:
+    return (-(-rows // 128) * 128) * (-(-(cols // 32) // 4) * 4)
+
+
+def _need(fn: str, name: str, t, nbytes: int) -> None:
+    """A torch tensor passed as a buffer must be a contiguous CUDA tensor on
+    the current device with at least nbytes; ints and None pass unchecked
+    (the C side rejects NULL)."""
+    if t is None or isinstance(t, int) or nbytes <= 0:
+        return
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{fn}: {name} must be a torch tensor or an integer device address")
+    if not t.is_cuda:
+        raise ValueError(f"{fn}: {name} is on {t.device}, not on a CUDA device")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{fn}: {name} is on {t.device}, but cuda:{torch.cuda.current_device()} is current")
+    if not t.is_contiguous():
+        raise ValueError(f"{fn}: {name} is not contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{fn}: {name} holds {have} bytes, the call needs {nbytes}")
+
+
+def _row_shape_ok(rows: int, cols: int) -> bool:
+    return rows > 0 and cols >= 32 and cols % 32 == 0 and cols <= 16384
+
+
+def _gemm_shape_ok(M: int, N: int, K: int) -> bool:
+    return M > 0 and N >= 16 and N % 16 == 0 and K >= 32 and K % 32 == 0
+
+
 # ------------------------------------------------------------- C entry points
 
 def mx_scale_bytes(rows: int, cols: int) -> int:
@@ -121,52 +161,108 @@ def mx_scale_bytes(rows: int, cols: int) -> int:
 
 
 def mx_rmsnorm_quant(x, w, eps: float, out_q, out_scales, M: int, H: int, stream=None) -> None:
+    if _row_shape_ok(M, H):
+        fn = "mx_rmsnorm_quant"
+        _need(fn, "x", x, 2 * M * H)
+        _need(fn, "w", w, 2 * H)
+        _need(fn, "out_q", out_q, M * H)
+        _need(fn, "out_scales", out_scales, _scale_bytes_py(M, H))
     _check("mx_rmsnorm_quant", lib().mx_rmsnorm_quant(_ptr(x), _ptr(w), float(eps), _ptr(out_q), _ptr(out_scales),
                                                       M, H, _stream(stream, x)))
 
 
 def mx_rmsnorm_quant_ex(x, w, eps: float, out_q, out_scales, M: int, H: int, scale_layout: int,
                         stream=None) -> None:
+    if _row_shape_ok(M, H) and scale_layout in (MX_SCALES_F8_128X4, MX_SCALES_ROW_MAJOR):
+        fn = "mx_rmsnorm_quant_ex"
+        _need(fn, "x", x, 2 * M * H)
+        _need(fn, "w", w, 2 * H)
+        _need(fn, "out_q", out_q, M * H)
+        _need(fn, "out_scales", out_scales,
+              M * (H // 32) if scale_layout == MX_SCALES_ROW_MAJOR else _scale_bytes_py(M, H))
     _check("mx_rmsnorm_quant_ex", lib().mx_rmsnorm_quant_ex(_ptr(x), _ptr(w), float(eps), _ptr(out_q),
                                                             _ptr(out_scales), M, H, scale_layout,
                                                             _stream(stream, x)))
 
 
 def mx_rmsnorm_bf16(x, w, eps: float, out, M: int, H: int, stream=None) -> None:
+    if _row_shape_ok(M, H):
+        fn = "mx_rmsnorm_bf16"
+        _need(fn, "x", x, 2 * M * H)
+        _need(fn, "w", w, 2 * H)
+        _need(fn, "out", out, 2 * M * H)
     _check("mx_rmsnorm_bf16", lib().mx_rmsnorm_bf16(_ptr(x), _ptr(w), float(eps), _ptr(out), M, H,
                                                     _stream(stream, x)))
 
 
 def mx_swizzle_scales(in_row_major, out_swizzled, rows: int, cols: int, stream=None) -> None:
+    if _row_shape_ok(rows, cols):
+        _need("mx_swizzle_scales", "in_row_major", in_row_major, rows * (cols // 32))
+        _need("mx_swizzle_scales", "out_swizzled", out_swizzled, _scale_bytes_py(rows, cols))
     _check("mx_swizzle_scales", lib().mx_swizzle_scales(_ptr(in_row_major), _ptr(out_swizzled), rows, cols,
                                                         _stream(stream, in_row_major)))
 
 
 def mx_unswizzle_scales(in_swizzled, out_row_major, rows: int, cols: int, stream=None) -> None:
+    if _row_shape_ok(rows, cols):
+        _need("mx_unswizzle_scales", "in_swizzled", in_swizzled, _scale_bytes_py(rows, cols))
+        _need("mx_unswizzle_scales", "out_row_major", out_row_major, rows * (cols // 32))
     _check("mx_unswizzle_scales", lib().mx_unswizzle_scales(_ptr(in_swizzled), _ptr(out_row_major), rows, cols,
                                                             _stream(stream, in_swizzled)))
 
 
 def mx_quant_weights(x, out_q, out_scales, rows: int, cols: int, stream=None) -> None:
+    if _row_shape_ok(rows, cols):
+        fn = "mx_quant_weights"
+        _need(fn, "x", x, 2 * rows * cols)
+        _need(fn, "out_q", out_q, rows * cols)
+        _need(fn, "out_scales", out_scales, _scale_bytes_py(rows, cols))
     _check("mx_quant_weights", lib().mx_quant_weights(_ptr(x), _ptr(out_q), _ptr(out_scales), rows, cols,
                                                       _stream(stream, x)))
 
 
+def _need_gemm_inputs(fn, a_q, a_s, b_q, b_s, M, N, K):
+    _need(fn, "a_q", a_q, M * K)
+    _need(fn, "a_s", a_s, _scale_bytes_py(M, K))
+    _need(fn, "b_q", b_q, N * K)
+    _need(fn, "b_s", b_s, _scale_bytes_py(N, K))
+
+
 def mx_gemm(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, stream=None) -> None:
+    if _gemm_shape_ok(M, N, K):
+        _need_gemm_inputs("mx_gemm", a_q, a_s, b_q, b_s, M, N, K)
+        _need("mx_gemm", "out", out, 2 * M * N)
     _check("mx_gemm", lib().mx_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K,
                                     _stream(stream, a_q)))
 
 
 def mx_gemm_ex(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, tile_m: int = 0, tile_n: int = 0,
                stream=None) -> None:
+    if _gemm_shape_ok(M, N, K):
+        _need_gemm_inputs("mx_gemm_ex", a_q, a_s, b_q, b_s, M, N, K)
+        _need("mx_gemm_ex", "out", out, 2 * M * N)
     _check("mx_gemm_ex", lib().mx_gemm_ex(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K,
                                           tile_m, tile_n, _stream(stream, a_q)))
 
 
 def mx_gemm_quant(a_q, a_s, b_q, b_s, out_q, out_scales, M: int, N: int, K: int, tile_m: int = 0,
                   tile_n: int = 0, stream=None) -> None:
+    if _gemm_shape_ok(M, N, K) and N % 32 == 0:
+        _need_gemm_inputs("mx_gemm_quant", a_q, a_s, b_q, b_s, M, N, K)
+        _need("mx_gemm_quant", "out_q", out_q, M * N)
+        _need("mx_gemm_quant", "out_scales", out_scales, _scale_bytes_py(M, N))
     _check("mx_gemm_quant", lib().mx_gemm_quant(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out_q),
                                                 _ptr(out_scales), M, N, K, tile_m, tile_n, _stream(stream, a_q)))
+
+
+def mx_gemm_selftest_stall(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, tile_m: int = 0, tile_n: int = 0,
+                           wait_ns: int = 2_000_000, stream=None) -> None:
+    if _gemm_shape_ok(M, N, K):
+        _need_gemm_inputs("mx_gemm_selftest_stall", a_q, a_s, b_q, b_s, M, N, K)
+        _need("mx_gemm_selftest_stall", "out", out, 2 * M * N)
+    _check("mx_gemm_selftest_stall", lib().mx_gemm_selftest_stall(
+        _ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K, tile_m, tile_n, int(wait_ns),
+        _stream(stream, a_q)))
 
 
 def mx_gemm_plan(M: int, N: int, K: int):
@@ -177,6 +273,9 @@ def mx_gemm_plan(M: int, N: int, K: int):
 
 
 def mx_e4m3_encode_f32(inp, out, n: int, stream=None) -> None:
+    if n > 0:
+        _need("mx_e4m3_encode_f32", "inp", inp, 4 * n)
+        _need("mx_e4m3_encode_f32", "out", out, n)
     _check("mx_e4m3_encode_f32", lib().mx_e4m3_encode_f32(_ptr(inp), _ptr(out), n, _stream(stream, inp)))
 
 

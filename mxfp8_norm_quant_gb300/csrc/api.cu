@@ -82,14 +82,19 @@ mx_status check_gemm(int64_t M, int64_t N, int64_t K) {
 
 namespace mxk {
 
+// The table remembers the limit set per (kernel, device); once it is full
+// (more than TABLE kernel-device pairs, far beyond this library's ~40
+// kernels on 8 devices) the attribute is simply set on every call, which is
+// correct but slower.
 cudaError_t set_smem_once(const void* kernel, int bytes) {
   struct Entry {
     const void* fn;
     int dev;
     int bytes;
   };
+  constexpr int TABLE = 1024;
   static std::mutex mu;
-  static Entry table[256];
+  static Entry table[TABLE];
   static int used = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -103,7 +108,7 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
       return e;
     }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && used < 256) table[used++] = Entry{kernel, dev, bytes};
+  if (e == cudaSuccess && used < TABLE) table[used++] = Entry{kernel, dev, bytes};
   return e;
 }
 
@@ -225,6 +230,27 @@ MX_API mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s, const uint8_
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MX_API mx_status mx_gemm_selftest_stall(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q,
+                                        const uint8_t* b_s, void* out, int64_t M, int64_t N, int64_t K, int tile_m,
+                                        int tile_n, uint64_t wait_ns, mx_stream_t stream) {
+  mx_status st = check_gemm(M, N, K);
+  if (st != MX_OK) return st;
+  if (M == 0 || wait_ns < 100000ull || wait_ns > 1000000000ull) return MX_ERR_SHAPE;
+  const bool autotile = tile_m == 0 && tile_n == 0;
+  if (!autotile && !mxk::gemm_tile_supported(tile_m, tile_n)) return MX_ERR_SHAPE;
+  if (!a_q || !a_s || !b_q || !b_s || !out) return MX_ERR_NULL;
+  if (misaligned(a_q) || misaligned(a_s) || misaligned(b_q) || misaligned(b_s) || misaligned(out))
+    return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  if (autotile)
+    mxk::gemm_pick_tile(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), d->num_sms, &tile_m, &tile_n);
+  return launched(mxk::launch_gemm_stalled(a_q, a_s, b_q, b_s, out, static_cast<int>(M), static_cast<int>(N),
+                                           static_cast<int>(K), tile_m, tile_n, d->num_sms, d->fault, wait_ns,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MX_API mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s,
                                uint8_t* out_q, uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int tile_m,
                                int tile_n, mx_stream_t stream) {
@@ -285,8 +311,12 @@ MX_API mx_status mx_device_fault(uint32_t* code) {
   const DeviceInfo* d = nullptr;
   mx_status st = current_device(&d);
   if (st != MX_OK) return st;
+  // every kernel of the device, on every stream (non-blocking ones included),
+  // has finished before the word is read and cleared
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
   unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_mx_fault_word, sizeof(v));
+  e = cudaMemcpyFromSymbol(&v, g_mx_fault_word, sizeof(v));
   if (e != cudaSuccess) return cuda_fail(e);
   if (v != 0) {
     const unsigned int zero = 0;

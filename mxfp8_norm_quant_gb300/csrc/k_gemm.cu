@@ -54,6 +54,7 @@
 // offset 2 (tile widths are multiples of 64: an odd column offset is not a
 // valid scale address).  With cta_group::2 each CTA's TMEM holds the A scales
 // of its own rows and the B scales of the whole tile.
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -116,6 +117,8 @@ struct GemmArgs {
   int M, N, K;
   int tiles_m, tiles_n, k_tiles;  // tiles_m counts output tiles of Cfg::TM rows
   int out_32b_aligned;            // 32-byte vector stores are allowed
+  int withhold;                   // test hook: the producer issues no copies, so every wait runs out
+  unsigned long long wait_ns;     // limit of each bounded wait
   unsigned int* fault;
 };
 
@@ -249,6 +252,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t bar_last = bar_final + 16;  // the epilogue warps have reached the CTA's last tile
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+  // tiles the epilogue warps of this CTA have drained (helpers' stall clock)
+  volatile uint32_t* progress = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_ABORT + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -271,6 +276,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(bar_final + 8, 1);
     mbar_init(bar_last, 4);
     *abort_flag = 0;
+    *progress = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -304,13 +310,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // stage s and its phase parity ph advance together; `it` counts stages issued
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
-      for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
+      for (int tile = unit; tile < num_tiles && ok && !p.withhold; tile += nunits) {
         const int mt = tile / p.tiles_n, nt = tile % p.tiles_n;
         const int m0 = mt * C::TM + static_cast<int>(rank) * BM;
         const int n0 = nt * BN;
         const int b0 = n0 + static_cast<int>(rank) * C::B_ROWS;
         for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.wait_ns)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_PRODUCER);
             *abort_flag = 1;
             ok = false;
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           break;
         }
         const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, abort_flag)) {
+        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, abort_flag, p.wait_ns)) {
           if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
           *abort_flag = 1;
           break;
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t d_tmem = tmem + acc * BN;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           // the stage's operands have landed and its scales are in TMEM (every CTA of the tile)
-          if (!mbar_wait(bar_sfready + 8 * s, ph, abort_flag)) {
+          if (!mbar_wait(bar_sfready + 8 * s, ph, abort_flag, p.wait_ns)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
             *abort_flag = 1;
             ok = false;
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int tile = unit; tile < num_tiles && ok; tile += nunits) {
         for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, p.wait_ns)) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
             *abort_flag = 1;
             ok = false;
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int tile = unit; tile < num_tiles; tile += nunits) {
       bool ok = true;
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        if (!warp_wait(bar_full + 8 * s, ph, abort_flag)) {
+        if (!warp_wait(bar_full + 8 * s, ph, abort_flag, p.wait_ns)) {
           if (lane == 0) {
             if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_SCALES);
             *abort_flag = 1;
@@ -504,9 +510,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
       // a helper waits until the epilogue warps have reached the last tile:
       // then that tile's phase is the last one bar_tfull completes, and the
-      // parity wait cannot be satisfied by an earlier phase
-      bool ok = !helper || warp_wait(bar_last, 0, abort_flag);
-      ok = ok && warp_wait(bar_tfull + 8 * acc, aph, abort_flag);
+      // parity wait cannot be satisfied by an earlier phase.  That wait spans
+      // the CTA's whole run, so its limit bounds a stall of the epilogue
+      // warps' progress, not the run's length.
+      bool ok = !helper || warp_wait_progress(bar_last, 0, abort_flag, progress, p.wait_ns);
+      ok = ok && warp_wait(bar_tfull + 8 * acc, aph, abort_flag, p.wait_ns);
       if (!ok) {
         if (lane == 0) {
           if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_EPILOGUE);
@@ -532,6 +540,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!helper) {
         tc_fence_before();
         __syncwarp();
+        if (warp == 2 && lane == 0) *progress = tc + 1;
         if (lane == 0) {
           if constexpr (PAIR) {
             mbar_arrive_cluster(lead_tempty + 8 * acc);
@@ -606,13 +615,16 @@ cudaError_t make_scale_map(CUtensorMap* map, const uint8_t* ptr, int blocks, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Clusters of two that can be resident at once (cached per device and width).
+// Clusters of two that can be resident at once (cached per device and width;
+// concurrent first calls compute the same value, and the atomic makes the
+// publication race-free).
 template <int BN>
 int pair_max_clusters(int num_sms) {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
-  if (cached[dev] > 0) return cached[dev];
+  const int known = cached[dev].load(std::memory_order_acquire);
+  if (known > 0) return known;
   // both output forms have the same shared memory and block: one answer serves both
   auto kern = k_gemm_mxf8<BN, true, GEMM_OUT_BF16>;
   using C = Cfg<BN, true>;
@@ -623,14 +635,14 @@ int pair_max_clusters(int num_sms) {
     cudaGetLastError();
     n = num_sms / 2;
   }
-  cached[dev] = n;
+  cached[dev].store(n, std::memory_order_release);
   return n;
 }
 
 template <int BN, bool PAIR, int OUT>
 cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
                         uint8_t* q, uint8_t* qs, int M, int N, int K, int num_sms, unsigned int* fault,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int withhold, unsigned long long wait_ns) {
   using C = Cfg<BN, PAIR>;
   CUtensorMap ta, tb, tsa, tsb;
   const int k_tiles = (K + BK - 1) / BK;
@@ -654,6 +666,8 @@ cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq,
   // multiples of 32 (N % 32 == 0).  So the base alone decides.
   const void* vec_base = OUT == GEMM_OUT_MXFP8 ? static_cast<const void*>(q) : out;
   p.out_32b_aligned = (reinterpret_cast<uintptr_t>(vec_base) & 31u) == 0 ? 1 : 0;
+  p.withhold = withhold;
+  p.wait_ns = wait_ns;
   p.fault = fault;
   auto kern = k_gemm_mxf8<BN, PAIR, OUT>;
   err = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
@@ -737,18 +751,29 @@ namespace {
 template <int OUT>
 cudaError_t dispatch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
                           uint8_t* q, uint8_t* qs, int M, int N, int K, int tile_m, int tile_n, int num_sms,
-                          unsigned int* fault, cudaStream_t stream) {
+                          unsigned int* fault, cudaStream_t stream, int withhold = 0,
+                          unsigned long long wait_ns = WAIT_LIMIT_NS) {
   if (tile_m == 256) {
     switch (tile_n) {
-      case 128: return launch_tile<128, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
-      case 192: return launch_tile<192, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
+      case 128:
+        return launch_tile<128, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                           wait_ns);
+      case 192:
+        return launch_tile<192, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                           wait_ns);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (tile_n) {
-    case 64: return launch_tile<64, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
-    case 128: return launch_tile<128, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
-    case 192: return launch_tile<192, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream);
+    case 64:
+      return launch_tile<64, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                         wait_ns);
+    case 128:
+      return launch_tile<128, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                          wait_ns);
+    case 192:
+      return launch_tile<192, false, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                          wait_ns);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -759,6 +784,13 @@ cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq,
                         int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream) {
   return dispatch_tile<GEMM_OUT_BF16>(aq, as, bq, bs, out, nullptr, nullptr, M, N, K, tile_m, tile_n, num_sms, fault,
                                       stream);
+}
+
+cudaError_t launch_gemm_stalled(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
+                                int M, int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault,
+                                unsigned long long wait_ns, cudaStream_t stream) {
+  return dispatch_tile<GEMM_OUT_BF16>(aq, as, bq, bs, out, nullptr, nullptr, M, N, K, tile_m, tile_n, num_sms, fault,
+                                      stream, 1, wait_ns);
 }
 
 cudaError_t launch_gemm_quant(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, uint8_t* q,

@@ -60,6 +60,12 @@ void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n);
 int gemm_grid(int M, int N, int tile_m, int tile_n, int num_sms);
 cudaError_t launch_gemm(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out, int M,
                         int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault, cudaStream_t stream);
+// test hook: the GEMM launched with its producer issuing no copies, so that
+// every bounded wait runs out after wait_ns and the kernel takes its give-up
+// path (fault bits set, TMEM freed, clean exit); C is not written
+cudaError_t launch_gemm_stalled(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, void* out,
+                                int M, int N, int K, int tile_m, int tile_n, int num_sms, unsigned int* fault,
+                                unsigned long long wait_ns, cudaStream_t stream);
 // the same GEMM with C leaving as an MXFP8 operand (codes + F8_128x4 scales); N % 32 == 0
 cudaError_t launch_gemm_quant(const uint8_t* aq, const uint8_t* as, const uint8_t* bq, const uint8_t* bs, uint8_t* q,
                               uint8_t* qs, int M, int N, int K, int tile_m, int tile_n, int num_sms,

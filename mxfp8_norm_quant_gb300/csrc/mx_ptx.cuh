@@ -97,11 +97,47 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // Warp-uniform bounded wait: lane 0 waits, then every lane observes the
 // completed phase itself (so each thread gets the barrier's acquire
 // ordering); the result is the same in all 32 lanes.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  if (ok) ok = mbar_wait(bar, parity, abort);
+  if (ok) ok = mbar_wait(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+}
+
+// Bounded wait for a phase that may legitimately be far off (a whole CTA's
+// run of tiles): the time limit counts from the last change of *progress, a
+// counter the threads being waited for advance as they work, so it bounds a
+// stall, not the length of the run.  Same result in all 32 lanes.
+__device__ __forceinline__ bool warp_wait_progress(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                   const volatile uint32_t* progress, uint64_t limit_ns) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+    uint64_t t0 = globaltimer_ns();
+    uint32_t seen = *progress;
+    while (true) {
+      bool done = false;
+#pragma unroll 1
+      for (int i = 0; i < 32 && !done; ++i) done = mbar_try_wait(bar, parity);
+      if (done) break;
+      if (*abort != 0) {
+        ok = false;
+        break;
+      }
+      const uint64_t now = globaltimer_ns();
+      const uint32_t p = *progress;
+      if (p != seen) {
+        seen = p;
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) ok = mbar_wait(bar, parity, abort, limit_ns);
   return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 

@@ -305,22 +305,9 @@ def mx_decode(q: np.ndarray, s_swizzled: np.ndarray) -> np.ndarray:
     return (e4m3_decode(q).reshape(rows, c, BLOCK) * scale[:, :, None]).reshape(rows, cols)
 
 
-def gemm_ref(a_q, a_s, b_q, b_s, rows=None) -> np.ndarray:
+def gemm_ref(a_q, a_s, b_q, b_s) -> np.ndarray:
     """float64 reference of C = dec(A) . dec(B)^T (R7).
 
     a_q: (M, K) codes, a_s: swizzled A scales; b_q: (N, K), b_s likewise.
-    rows: optional index array of A rows to evaluate (sampled checks at full
-    size); the scales of those rows are looked up in the full A layout.
     """
-    b = mx_decode(b_q, b_s)
-    if rows is None:
-        a = mx_decode(a_q, a_s)
-    else:
-        rows = np.asarray(rows, dtype=np.int64)
-        k = a_q.shape[1]
-        c = k // BLOCK
-        rr, cc = np.meshgrid(rows, np.arange(c), indexing="ij")
-        sb = np.asarray(a_s, dtype=np.uint8).reshape(-1)[swizzle_offset(rr, cc, c)]
-        a = (e4m3_decode(np.asarray(a_q)[rows]).reshape(len(rows), c, BLOCK)
-             * ue8m0_decode(sb)[:, :, None]).reshape(len(rows), k)
-    return a @ b.T
+    return mx_decode(a_q, a_s) @ mx_decode(b_q, b_s).T

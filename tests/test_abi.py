@@ -144,6 +144,34 @@ def test_gemm_quant_rejects(lib):
     assert _status("mx_gemm_quant", None, None, None, None, None, None, 0, 256, 256, 0, 0, None) == 0
 
 
+def test_gemm_selftest_stall_rejects(lib):
+    args = [GOOD] * 5
+    u64 = ctypes.c_uint64
+    # the wait limit must lie in [100 us, 1 s]; M >= 1; shapes and tiles as for mx_gemm_ex
+    assert _status("mx_gemm_selftest_stall", *args, 128, 256, 256, 0, 0, u64(99_999), None) == 3
+    assert _status("mx_gemm_selftest_stall", *args, 128, 256, 256, 0, 0, u64(1_000_000_001), None) == 3
+    assert _status("mx_gemm_selftest_stall", *args, 0, 256, 256, 0, 0, u64(2_000_000), None) == 3
+    assert _status("mx_gemm_selftest_stall", *args, 128, 8, 256, 0, 0, u64(2_000_000), None) == 3
+    assert _status("mx_gemm_selftest_stall", *args, 128, 256, 256, 256, 64, u64(2_000_000), None) == 3
+    for i in range(5):
+        a = list(args)
+        a[i] = None
+        assert _status("mx_gemm_selftest_stall", *a, 128, 256, 256, 0, 0, u64(2_000_000), None) == 1
+        a[i] = GOOD + 8
+        assert _status("mx_gemm_selftest_stall", *a, 128, 256, 256, 0, 0, u64(2_000_000), None) == 2
+
+
+def test_binding_checks_tensor_buffers(lib):
+    # a CPU tensor, or one too small for the call, is refused on the host
+    # before its address reaches the library
+    import torch
+    small = torch.empty(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        mx.mx_quant_weights(small, GOOD, GOOD, 4, 64)
+    with pytest.raises(ValueError):
+        mx.mx_gemm(small, GOOD, GOOD, GOOD, GOOD, 128, 256, 256)
+
+
 def test_e4m3_probe_and_fault_reject(lib):
     assert _status("mx_e4m3_encode_f32", GOOD, GOOD, -1, None) == 3
     assert _status("mx_e4m3_encode_f32", None, GOOD, 4, None) == 1
