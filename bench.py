@@ -2,13 +2,22 @@
 
 One step = one pass of the whole path over one batch of M tokens:
   1. fused Gemma RMSNorm + MXFP8 quantisation of the residual x (M x 6144),
-  2. MXFP8 quantisation of the o_proj activation A (M x 2048) and its GEMM
-     against the pre-quantised weight W (6144 x 2048), bf16 out,
-  3. the same for the down_proj activation (M x 3072) and W (6144 x 3072).
+  2. per contraction K of the workload: MXFP8 quantisation of the activation
+     A (M x K) and its GEMM against the pre-quantised weight W (6144 x K),
+     bf16 out.
 Weights are quantised once, before timing (serving loads MXFP8 weights).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload m1024]
+The default workload is the largest single-GPU configuration, m32768_stress:
+32768 tokens, the down_proj GEMM (K = 3072) and the 32768 x 6144 stress
+residual (outlier channels, zero blocks, a zero row).  The same JSON line
+carries a `sweep` record: every (M, K) point of the M sweep (M = 128 ...
+32768, K = 2048 and 3072) and the m4096_rowscale workload, each kernel timed
+alone (GEMM TFLOP/s and fraction of FP8 peak, norm-quant and quant GB/s and
+fraction of HBM bandwidth).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload m32768_stress]
     python bench.py --impl reference ...   # the CPU oracle, timed on a bounded sample
+    python bench.py --kernel gemm --workload sweep_m4096_k3072   # one kernel alone
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs the same
 per-GPU workload on its own batch (weak scaling, no collective on the data
@@ -18,6 +27,7 @@ path); the barrier-bracketed time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -35,6 +45,8 @@ N_OUT = 6144
 EPS = 1e-6
 L2_BYTES = 129 * 1024 * 1024
 FP8_PER_BF16 = 2.0        # dense FP8 / dense BF16 tensor rate (4.5 / 2.25 PFLOP/s nominal)
+METRIC = "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144"
+DEFAULT_WORKLOAD = "m32768_stress"
 
 
 def load_peaks():
@@ -50,22 +62,21 @@ def load_peaks():
 
 # ------------------------------------------------------------------ measured DRAM traffic
 
-def gemm_traffic_per_step(workload):
-    """DRAM bytes (read + write) of the step's GEMM launches from the ncu
-    capture committed under profiles/, or None when that capture is of
-    another workload or of an earlier version of the kernel source."""
-    import hashlib
-    path = os.path.join(ROOT, "profiles", "k_gemm_mxf8_m1024_traffic.json")
+def gemm_traffic_per_launch(workload, k):
+    """DRAM bytes (read + write) of one GEMM launch of the workload from the
+    ncu capture committed under profiles/, or None when no capture of this
+    workload exists or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "k_gemm_mxf8_traffic.json")
     try:
-        rec = json.load(open(path))["k_gemm_mxf8"]
+        rec = json.load(open(path))
         h = hashlib.sha256()
         for f in rec["source_files"]:
             h.update(open(os.path.join(ROOT, f), "rb").read())
-    except (OSError, KeyError, ValueError):
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        return int(rec["workloads"][workload]["dram_bytes_per_launch"][str(k)])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    if h.hexdigest() != rec["source_sha256"] or workload != "m1024":
-        return None
-    return rec["dram_bytes_per_step"]
 
 
 # ------------------------------------------------------------------ traffic model
@@ -123,6 +134,15 @@ def aggregate_over_ranks(ms_per_step, work_per_step, world, device=None):
     return ms_max, world * work_per_step / (ms_max * 1e-3)
 
 
+def make_config(wl, world):
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": wl.name, "M": wl.m, "N": N_OUT, "K": list(wl.ks), "norm_quant": f"{wl.norm_rows}x{H}",
+            "step": "norm-quant(x) + per K: quant(A) + gemm(A, W pre-quantised)",
+            "l2": "inputs larger than L2: rotating input and weight sets of more than 2x L2 between "
+                  "consecutive launches of a buffer (no flush)",
+            "parallelism": f"weak, {world} independent rank(s)"}
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -136,7 +156,6 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.marks = []
 
     def start(self):
         try:
@@ -152,9 +171,6 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
-
-    def mark(self):
-        self.marks.append(time.time())
 
     def stop(self):
         if self.proc is not None:
@@ -185,6 +201,44 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ timing helpers
+
+def graph_time(torch, stream, launch, n, replays):
+    """Captures launch(0) ... launch(n-1) as one CUDA graph on `stream`,
+    replays it once untimed, then `replays` times, each bracketed by CUDA
+    events on the stream.  Returns the per-replay times in ms."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            launch(i)
+    times = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        stream.synchronize()
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            times.append(e0.elapsed_time(e1))
+    del g
+    return times
+
+
+def per_launch_stats(times_ms, n):
+    """Median, min and max time of one launch in µs from per-replay times of n launches."""
+    per = [t / n * 1e3 for t in times_ms]
+    return statistics.median(per), min(per), max(per)
+
+
+def rotation(bytes_per_launch):
+    """Launches per timed replay: enough that one replay moves more than
+    2.2x L2 through HBM, and at least 20."""
+    return max(20, math.ceil(2.2 * L2_BYTES / max(1, bytes_per_launch)))
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_gpu(args, rank, world):
@@ -201,28 +255,32 @@ def run_gpu(args, rank, world):
     ks = wl.ks
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
 
     # ---- inputs, resident in HBM; R rotating sets so that the working set of
     # consecutive steps exceeds L2 (no flush needed between steps)
     x_h, w_h = wl.norm(seed=rank)
-    a_h = {k: wl.gemm(k, seed=rank)[0] for k in ks}
-    wt_h = {k: wl.gemm(k, seed=rank)[1] for k in ks}
+    a_h, wt_h = {}, {}
+    for k in ks:
+        a_h[k], wt_h[k] = wl.gemm(k, seed=rank)
     w_dev = w_h.to(dev)
     wq = {}
     for k in ks:
         wd = wt_h[k].to(dev)
         wq[k] = mx.quant(wd)
         del wd
-    set_bytes = 2 * M * H + M * H + mx.mx_scale_bytes(M, H)
+    set_bytes = 2 * wl.norm_rows * H + wl.norm_rows * H + mx.mx_scale_bytes(wl.norm_rows, H)
     for k in ks:
         set_bytes += 3 * M * k + mx.mx_scale_bytes(M, k) + 2 * M * N_OUT
     weight_bytes = sum(N_OUT * k + mx.mx_scale_bytes(N_OUT, k) for k in ks)
     R = max(2, math.ceil(2.2 * L2_BYTES / max(1, set_bytes + weight_bytes)))
     R = min(R, 16)
+    Mn = wl.norm_rows
     sets = []
     for r in range(R):
-        s = {"x": x_h.to(dev), "q": torch.empty((M, H), dtype=torch.uint8, device=dev),
-             "s": torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)}
+        s = {"x": x_h.to(dev), "q": torch.empty((Mn, H), dtype=torch.uint8, device=dev),
+             "s": torch.empty(mx.mx_scale_bytes(Mn, H), dtype=torch.uint8, device=dev)}
         for k in ks:
             s[f"a{k}"] = a_h[k].to(dev)
             s[f"aq{k}"] = torch.empty((M, k), dtype=torch.uint8, device=dev)
@@ -233,31 +291,19 @@ def run_gpu(args, rank, world):
     wsets = [wq] + [{k: (wq[k][0].clone(), wq[k][1].clone()) for k in ks} for _ in range(R - 1)]
     torch.cuda.synchronize()
 
-    def step(i, ev=None):
+    def step(i):
         s = sets[i % R]
         wsx = wsets[i % R]
-        j = 0
-
-        def mark():
-            nonlocal j
-            if ev is not None:
-                ev[j].record(stream)
-            j += 1
-
-        mark()
-        mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], M, H, sptr)
-        mark()
+        mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], Mn, H, sptr)
         for k in ks:
             mx.mx_quant_weights(s[f"a{k}"], s[f"aq{k}"], s[f"as{k}"], M, k, sptr)
-            mark()
             mx.mx_gemm(s[f"aq{k}"], s[f"as{k}"], wsx[k][0], wsx[k][1], s[f"c{k}"], M, N_OUT, k, sptr)
-            mark()
 
     def one_kernel(i, idx):
         s = sets[i % R]
         wsx = wsets[i % R]
         if idx == 0:
-            mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], M, H, sptr)
+            mx.mx_rmsnorm_quant(s["x"], w_dev, EPS, s["q"], s["s"], Mn, H, sptr)
             return
         k = ks[(idx - 1) // 2]
         if (idx - 1) % 2 == 0:
@@ -265,7 +311,6 @@ def run_gpu(args, rank, world):
         else:
             mx.mx_gemm(s[f"aq{k}"], s[f"as{k}"], wsx[k][0], wsx[k][1], s[f"c{k}"], M, N_OUT, k, sptr)
 
-    n_marks = 2 + 2 * len(ks)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
@@ -274,23 +319,13 @@ def run_gpu(args, rank, world):
 
     # The K timed steps are captured once as a CUDA graph (the launches go
     # through the same C entry points; the graph removes the host's per-call
-    # launch latency, as a serving engine's CUDA-graph mode does).  For the
-    # per-kernel breakdown each kernel of the step also gets a graph of its K
-    # launches over the same rotating buffers, timed the same way.
+    # launch latency, as a serving engine's CUDA-graph mode does).  The graph
+    # is replayed `replays` times, each replay timed on its own; the step time
+    # is the median replay / K.
     g_main = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_main, stream=stream):
         for i in range(args.steps):
             step(i)
-    order = ["norm_quant"]
-    for k in ks:
-        order += [f"quant_a{k}", f"gemm_k{k}"]
-    g_kern = []
-    for idx in range(len(order)):
-        gk = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gk, stream=stream):
-            for i in range(args.steps):
-                one_kernel(i, idx)
-        g_kern.append(gk)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
@@ -299,45 +334,77 @@ def run_gpu(args, rank, world):
     t_soak = time.time()
     with torch.cuda.stream(stream):
         while time.time() - t_soak < 1.5:
-            for _ in range(5):
+            for _ in range(3):
                 g_main.replay()
             stream.synchronize()
 
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    replay_ms = []
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        g_main.replay()
-        e1.record(stream)
+        for _ in range(args.replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_main.replay()
+            e1.record(stream)
+            stream.synchronize()
+            replay_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t_wall1 = time.time()
-    total_ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(t_soak, t_wall1)
+    ms_per_step = statistics.median(replay_ms) / args.steps
 
-    # per-kernel durations: each kernel's graph of K launches, replayed once
+    # per-kernel durations: a graph of each kernel's K launches (same
+    # rotating buffers), replayed and timed the same way
+    order = ["norm_quant"]
+    for k in ks:
+        order += [f"quant_a{k}", f"gemm_k{k}"]
     per_kernel = {}
-    with torch.cuda.stream(stream):
-        for idx, name in enumerate(order):
-            b0 = torch.cuda.Event(enable_timing=True)
-            b1 = torch.cuda.Event(enable_timing=True)
-            b0.record(stream)
-            g_kern[idx].replay()
-            b1.record(stream)
-            stream.synchronize()
-            per_kernel[name] = b0.elapsed_time(b1)
-    breakdown_ms = sum(per_kernel.values())
-    torch.cuda.synchronize()
+    for idx, name in enumerate(order):
+        t = graph_time(torch, stream, lambda i: one_kernel(i, idx), args.steps, max(5, args.replays // 2))
+        per_kernel[name] = per_launch_stats(t, args.steps)
     sampler.stop()
     assert mx.mx_device_fault() == 0
-    ms_per_step = total_ms / args.steps
 
     flops_step = sum(gemm_flops(M, N_OUT, k) for k in ks)
-    gemm_ms = sum(per_kernel[f"gemm_k{k}"] for k in ks)
+    kern = {}
+    denom = sum(v[0] for v in per_kernel.values())
+    for name in order:
+        us, us_min, us_max = per_kernel[name]
+        rec = {"us": us, "us_min": us_min, "us_max": us_max, "share": us / denom}
+        if name == "norm_quant":
+            b = norm_quant_bytes(Mn)
+            rec.update({"GB/s": b / (us * 1e-6) / 1e9, "frac_hbm": b / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]})
+        elif name.startswith("quant_a"):
+            b = quant_bytes(M, int(name[7:]))
+            rec.update({"GB/s": b / (us * 1e-6) / 1e9, "frac_hbm": b / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]})
+        else:
+            f = gemm_flops(M, N_OUT, int(name[6:]))
+            rec.update({"TFLOP/s": f / (us * 1e-6) / 1e12, "frac_fp8": f / (us * 1e-6) / 1e12 / fp8_peak})
+        kern[name] = rec
+    plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
+
+    # the dominant kernel of the step and its roofline
+    dom = max(order, key=lambda n: per_kernel[n][0])
+    if dom.startswith("gemm_k"):
+        k = int(dom[6:])
+        roof = {"bound": "tensor", "achieved": kern[dom]["TFLOP/s"], "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": kern[dom]["frac_fp8"], "traffic": gemm_traffic_per_launch(wl.name, k),
+                "kernel": f"k_gemm_mxf8, {M}x{N_OUT}x{k}, one launch per step",
+                "algorithmic": {"flops_per_launch": gemm_flops(M, N_OUT, k),
+                                "bytes_per_launch": gemm_bytes(M, N_OUT, k)},
+                "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_PER_BF16} "
+                               "(nominal dense FP8/BF16 ratio), of measured"}
+    else:
+        b = norm_quant_bytes(Mn) if dom == "norm_quant" else quant_bytes(M, int(dom[7:]))
+        roof = {"bound": "hbm", "achieved": kern[dom]["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": kern[dom]["frac_hbm"], "traffic": None, "kernel": dom,
+                "algorithmic": {"bytes_per_launch": b}, "peak_source": f"{peaks['source']} HBM copy"}
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks)
@@ -345,34 +412,17 @@ def run_gpu(args, rank, world):
     # ---- aggregate over ranks: max time, sum of work
     ms_max, value = aggregate_over_ranks(ms_per_step, flops_step / 1e12, world, dev)
 
-    peaks = load_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
-    gemm_tflops = flops_step * args.steps / (gemm_ms * 1e-3) / 1e12
-    nq_ms = per_kernel["norm_quant"] / args.steps
-    nq_gbs = norm_quant_bytes(M) / (nq_ms * 1e-3) / 1e9
-    kern = {}
-    denom = breakdown_ms
-    for name in order:
-        ms = per_kernel[name] / args.steps
-        if name == "norm_quant":
-            b = norm_quant_bytes(M)
-            kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
-                          peaks["hbm_gbs"], "share": per_kernel[name] / denom}
-        elif name.startswith("quant_a"):
-            k = int(name[7:])
-            b = quant_bytes(M, k)
-            kern[name] = {"us": ms * 1e3, "GB/s": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 /
-                          peaks["hbm_gbs"], "share": per_kernel[name] / denom}
-        else:
-            k = int(name[6:])
-            f = gemm_flops(M, N_OUT, k)
-            kern[name] = {"us": ms * 1e3, "TFLOP/s": f / (ms * 1e-3) / 1e12,
-                          "frac_fp8": f / (ms * 1e-3) / 1e12 / fp8_peak, "share": per_kernel[name] / denom}
-    plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
+    del sets, wsets, wq, g_main
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    sweep = None
+    if not args.no_sweep:
+        sweep = run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak)
+        assert mx.mx_device_fault() == 0
 
-    clocks = sampler.summary(t_soak, t_wall1)
+    nq = kern["norm_quant"]
     out = {
-        "metric": "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144",
+        "metric": METRIC,
         "value": value,
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -383,33 +433,180 @@ def run_gpu(args, rank, world):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "e4m3+ue8m0 in, fp32 accumulate, bf16 out",
-        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, U(-0.1,0.1) norm gain)",
-        "config": {"workload": wl.name, "M": M, "N": N_OUT, "K": list(ks), "norm_quant": f"{M}x{H}",
-                   "step": "norm-quant(x) + per K: quant(A) + gemm(A, W_pre-quantised)",
-                   "l2": f"{R} rotating input+weight sets, {(set_bytes + weight_bytes) * R / 2**20:.0f} MiB "
-                         f"total > L2 (no flush)",
-                   "parallelism": f"weak, {world} independent rank(s)", "gemm_plan": plan},
-        "gemm_tflops": gemm_tflops,
-        "norm_quant_gbs": nq_gbs,
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, U(-0.1,0.1) norm gain"
+                + ("; residual with 61 x50 outlier channels, 1/128 zero blocks, row 0 zero)" if wl.stress else ")"),
+        "config": make_config(wl, world),
+        "gemm_plan": plan,
+        "norm_quant_gbs": nq["GB/s"],
         "kernels": kern,
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp8_peak, "traffic": gemm_traffic_per_step(args.workload),
-                     "kernel": "k_gemm_mxf8 (both launches of the step)",
-                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x {FP8_PER_BF16} "
-                                    "(nominal dense FP8/BF16 ratio)"},
-        "norm_quant_roofline": {"bound": "hbm", "achieved": nq_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": nq_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]},
+        "roofline": roof,
+        "norm_quant_roofline": {"bound": "hbm", "achieved": nq["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": nq["frac_hbm"], "peak_source": f"{peaks['source']} HBM copy"},
         "e2e": e2e,
         "gpu_launches": len(order) * args.steps,
-        "timing": {"timed_region": "one CUDA-graph replay of the K steps (CUDA events on the launch stream)",
-                   "per_kernel": "one CUDA graph of the kernel's K launches per kernel (same rotating buffers), "
-                                 "CUDA events on the launch stream; shares are of the sum of these"},
+        "timing": {"timed_region": f"the K={args.steps}-step CUDA graph, replayed {args.replays} times, each "
+                                   "replay timed with CUDA events on the launch stream",
+                   "ms_per_step_median": ms_per_step,
+                   "ms_per_step_min": min(replay_ms) / args.steps,
+                   "ms_per_step_max": max(replay_ms) / args.steps,
+                   "gpu_launches_per_replay": len(order) * args.steps,
+                   "rotating_sets": R,
+                   "rotating_MiB": round((set_bytes + weight_bytes) * R / 2**20),
+                   "per_kernel": "a CUDA graph of the kernel's K launches (same rotating buffers), "
+                                 "replayed and timed the same way; us = median per launch"},
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
+    if sweep is not None:
+        out["sweep"] = sweep
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        out["cpu_baseline"] = cpu_baseline(wl, ks, budget_s=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(wl, ks)
     return out
+
+
+def run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak):
+    """Each kernel of the path timed alone at every point of the M sweep
+    (M = 128 ... 32768, K = 2048 and 3072, N = H = 6144) and on the
+    m4096_rowscale workload.  Inputs: the seeded 32768-row sweep tensors (the
+    first M rows are exactly the sweep_m<M> workload), held twice over in
+    one device pool; the launches of one timed replay cycle over row windows
+    of the pool (and over copies of the weight) so that every replay moves
+    more than 2.2x L2 through HBM."""
+    from mxfp8_norm_quant_gb300 import workloads as W
+    sptr = stream.cuda_stream
+    reps = args.sweep_replays
+    Mmax = max(W.M_SWEEP)
+    pool = 2 * Mmax
+    cp = (H // 32 + 3) // 4 * 4                      # scale bytes per row of a 6144-wide operand
+    pts = {}
+
+    def windows(m):
+        return pool // m                             # row windows of the pool at offsets j*m (j*m % 128 == 0)
+
+    # ---- norm-quant
+    x_h, w_h = W.norm_inputs(Mmax, H, seed=0)
+    x_pool = torch.empty((pool, H), dtype=torch.bfloat16, device=dev)
+    x_pool[:Mmax].copy_(x_h.to(dev))
+    x_pool[Mmax:].copy_(x_pool[:Mmax])
+    del x_h
+    q_pool = torch.empty((pool, H), dtype=torch.uint8, device=dev)
+    s_pool = torch.empty(pool * cp, dtype=torch.uint8, device=dev)
+    w_dev = w_h.to(dev)
+    norm_pts = []
+    for m in W.M_SWEEP:
+        nw = windows(m)
+        n = rotation(norm_quant_bytes(m))
+
+        def launch(i, m=m, nw=nw):
+            r0 = (i % nw) * m
+            mx.mx_rmsnorm_quant(x_pool[r0:r0 + m], w_dev, EPS, q_pool[r0:r0 + m], s_pool[r0 * cp:(r0 + m) * cp],
+                                m, H, sptr)
+        us, lo, hi = per_launch_stats(graph_time(torch, stream, launch, n, reps), n)
+        gbs = norm_quant_bytes(m) / (us * 1e-6) / 1e9
+        norm_pts.append({"M": m, "us": us, "us_min": lo, "us_max": hi, "GB/s": gbs,
+                         "frac_hbm": gbs / peaks["hbm_gbs"], "launches_per_replay": n})
+    del x_pool, q_pool, s_pool
+    torch.cuda.empty_cache()
+
+    # ---- quant + GEMM per K
+    gemm_pts = []
+    for k in (W.K_OPROJ, W.K_DOWN):
+        a_h, wt_h = W.gemm_operands(Mmax, k, seed=0)
+        a_pool = torch.empty((pool, k), dtype=torch.bfloat16, device=dev)
+        a_pool[:Mmax].copy_(a_h.to(dev))
+        a_pool[Mmax:].copy_(a_pool[:Mmax])
+        del a_h
+        cpk = (k // 32 + 3) // 4 * 4
+        aq_pool = torch.empty((pool, k), dtype=torch.uint8, device=dev)
+        as_pool = torch.empty(pool * cpk, dtype=torch.uint8, device=dev)
+        mx.mx_quant_weights(a_pool, aq_pool, as_pool, pool, k, sptr)
+        wq0 = mx.quant(wt_h.to(dev), stream=sptr)
+        wbytes = N_OUT * k + mx.mx_scale_bytes(N_OUT, k)
+        nwq = max(3, min(24, math.ceil(2.2 * L2_BYTES / wbytes)))
+        wqs = [wq0] + [(wq0[0].clone(), wq0[1].clone()) for _ in range(nwq - 1)]
+        c_pool = torch.empty((pool, N_OUT), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        for m in W.M_SWEEP:
+            nw = windows(m)
+            ng = rotation(gemm_bytes(m, N_OUT, k))
+
+            def lg(i, m=m, nw=nw):
+                r0 = (i % nw) * m
+                wq_ = wqs[i % nwq]
+                mx.mx_gemm(aq_pool[r0:r0 + m], as_pool[r0 * cpk:(r0 + m) * cpk], wq_[0], wq_[1],
+                           c_pool[r0:r0 + m], m, N_OUT, k, sptr)
+            us, lo, hi = per_launch_stats(graph_time(torch, stream, lg, ng, reps), ng)
+            tf = gemm_flops(m, N_OUT, k) / (us * 1e-6) / 1e12
+            nq_ = rotation(quant_bytes(m, k))
+
+            def lq(i, m=m, nw=nw):
+                r0 = (i % nw) * m
+                mx.mx_quant_weights(a_pool[r0:r0 + m], aq_pool[r0:r0 + m], as_pool[r0 * cpk:(r0 + m) * cpk],
+                                    m, k, sptr)
+            qus, qlo, qhi = per_launch_stats(graph_time(torch, stream, lq, nq_, reps), nq_)
+            qgbs = quant_bytes(m, k) / (qus * 1e-6) / 1e9
+            plan = mx.mx_gemm_plan(m, N_OUT, k)
+            gemm_pts.append({"M": m, "K": k, "gemm_us": us, "gemm_us_min": lo, "gemm_us_max": hi,
+                             "gemm_tflops": tf, "frac_fp8": tf / fp8_peak,
+                             "tile": [plan["tile_m"], plan["tile_n"]],
+                             "quant_us": qus, "quant_gbs": qgbs, "quant_frac_hbm": qgbs / peaks["hbm_gbs"]})
+        del a_pool, aq_pool, as_pool, wqs, wq0, c_pool
+        torch.cuda.empty_cache()
+
+    # ---- m4096_rowscale: LogUniform row scales on A and x
+    wl = W.WORKLOADS["m4096_rowscale"]
+    m = wl.m
+    rs = {}
+    xr, wr = wl.norm(seed=0)
+    nsets = max(3, math.ceil(2.2 * L2_BYTES / norm_quant_bytes(m)))
+    xs = [xr.to(dev) for _ in range(nsets)]
+    wrd = wr.to(dev)
+    qs = [torch.empty((m, H), dtype=torch.uint8, device=dev) for _ in range(nsets)]
+    ss = [torch.empty(mx.mx_scale_bytes(m, H), dtype=torch.uint8, device=dev) for _ in range(nsets)]
+
+    def ln(i):
+        j = i % nsets
+        mx.mx_rmsnorm_quant(xs[j], wrd, EPS, qs[j], ss[j], m, H, sptr)
+    n = rotation(norm_quant_bytes(m))
+    us, lo, hi = per_launch_stats(graph_time(torch, stream, ln, n, reps), n)
+    gbs = norm_quant_bytes(m) / (us * 1e-6) / 1e9
+    rs["norm_quant"] = {"M": m, "us": us, "us_min": lo, "us_max": hi, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    del xs, qs, ss
+    for k in wl.ks:
+        a, wt = wl.gemm(k, seed=0)
+        per = gemm_bytes(m, N_OUT, k)
+        nsets = max(3, math.ceil(2.2 * L2_BYTES / per))
+        ad = [a.to(dev) for _ in range(nsets)]
+        ops = [mx.quant(t, stream=sptr) for t in ad]
+        wqs = [mx.quant(wt.to(dev), stream=sptr) for _ in range(nsets)]
+        cs = [torch.empty((m, N_OUT), dtype=torch.bfloat16, device=dev) for _ in range(nsets)]
+
+        def lg(i, k=k):
+            j = i % nsets
+            mx.mx_gemm(ops[j][0], ops[j][1], wqs[j][0], wqs[j][1], cs[j], m, N_OUT, k, sptr)
+
+        def lq(i, k=k):
+            j = i % nsets
+            mx.mx_quant_weights(ad[j], ops[j][0], ops[j][1], m, k, sptr)
+        n = rotation(per)
+        us, lo, hi = per_launch_stats(graph_time(torch, stream, lg, n, reps), n)
+        tf = gemm_flops(m, N_OUT, k) / (us * 1e-6) / 1e12
+        n = rotation(quant_bytes(m, k))
+        qus, _, _ = per_launch_stats(graph_time(torch, stream, lq, n, reps), n)
+        qgbs = quant_bytes(m, k) / (qus * 1e-6) / 1e9
+        rs[f"k{k}"] = {"gemm_us": us, "gemm_us_min": lo, "gemm_us_max": hi, "gemm_tflops": tf,
+                       "frac_fp8": tf / fp8_peak, "quant_us": qus, "quant_gbs": qgbs,
+                       "quant_frac_hbm": qgbs / peaks["hbm_gbs"]}
+        del ad, ops, wqs, cs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"note": "each kernel alone: a CUDA graph of >= 20 launches cycling over row windows of a "
+                    "device pool holding the seeded 32768-row sweep tensors twice (the first M rows are the "
+                    f"sweep_m<M> workload) and over weight copies, > 2.2x L2 per replay; {reps} timed replays, "
+                    "us = median per launch (min, max over replays)",
+            "peaks": {"fp8_tflops": fp8_peak, "hbm_gbs": peaks["hbm_gbs"],
+                      "source": f"{peaks['source']}; FP8 = bf16 x {FP8_PER_BF16}"},
+            "gemm_quant": gemm_pts, "norm_quant": norm_pts, "m4096_rowscale": rs}
 
 
 def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
@@ -421,13 +618,14 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
     compute overlaps step i+1's copy-in and step i-1's copy-out.  The timed
     region runs from before the first copy-in to after the last copy-out."""
     M = wl.m
+    Mn = wl.norm_rows
     x_pin = x_h.pin_memory()
     a_pin = {k: a_h[k].pin_memory() for k in ks}
 
     def buffers():
         b = {"x": torch.empty_like(x_pin, device=dev),
-             "q": torch.empty((M, H), dtype=torch.uint8, device=dev),
-             "s": torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=dev)}
+             "q": torch.empty((Mn, H), dtype=torch.uint8, device=dev),
+             "s": torch.empty(mx.mx_scale_bytes(Mn, H), dtype=torch.uint8, device=dev)}
         for k in ks:
             b[f"a{k}"] = torch.empty_like(a_pin[k], device=dev)
             b[f"aq{k}"] = torch.empty((M, k), dtype=torch.uint8, device=dev)
@@ -465,7 +663,7 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
         s_comp.wait_event(in_done[j])
         s_comp.wait_event(out_done[j])
         sp = s_comp.cuda_stream
-        mx.mx_rmsnorm_quant(b["x"], w_dev, EPS, b["q"], b["s"], M, H, sp)
+        mx.mx_rmsnorm_quant(b["x"], w_dev, EPS, b["q"], b["s"], Mn, H, sp)
         for k in ks:
             mx.mx_quant_weights(b[f"a{k}"], b[f"aq{k}"], b[f"as{k}"], M, k, sp)
             mx.mx_gemm(b[f"aq{k}"], b[f"as{k}"], wq[k][0], wq[k][1], b[f"c{k}"], M, N_OUT, k, sp)
@@ -488,10 +686,12 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
     for i in range(args.steps):
         step(i)
     s_out.wait_event(comp_done[(args.steps - 1) % 2])
+    s_out.wait_event(out_done[(args.steps - 1) % 2])
     e1.record(s_out)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     flops = sum(gemm_flops(M, N_OUT, k) for k in ks)
+    del bufs
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": "copy-in, compute and copy-out streams, double-buffered device and pinned host buffers"}
@@ -499,7 +699,7 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
 
 # ------------------------------------------------------------------ CPU oracle arm
 
-def _oracle_threads():
+def _blas_threads():
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -507,26 +707,79 @@ def _oracle_threads():
             return max(n)
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return None
+
+
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_baseline(wl, ks, sample_rows=(256, 1024), chunk=4096):
+    """The oracle as it stands, on the host cores, on the headline workload:
+    the norm-quant over all of x (in row chunks, so the temporaries stay a
+    few GB), and quant + GEMM of the first r rows of each A against the full
+    weight for the two sample sizes r in `sample_rows`.  The quant + GEMM
+    time is extrapolated to all M rows by the straight line through the two
+    samples (a fixed part -- the GEMM decodes the whole weight each call --
+    plus a per-row part); the extrapolation is labelled as such.  The norm
+    and the quantiser run in numpy on one thread; the GEMM's float64 matmul
+    uses the BLAS threads."""
+    import oracle as O
+    x, w = wl.norm(seed=0)
+    xb, wb = _bits(x), _bits(w)
+    Mn = xb.shape[0]
+    t0 = time.time()
+    for r in range(0, Mn, chunk):
+        O.rmsnorm_quant(xb[r:r + chunk], wb, wl.eps)
+    t_norm = time.time() - t0
+    per_k = {}
+    t_full = t_norm
+    r1, r2 = sample_rows
+    for k in ks:
+        a, wt = wl.gemm(k, seed=0)
+        bq, bs = O.quant(_bits(wt))                       # untimed: weights are pre-quantised
+        ts = []
+        for r in (r1, r2):
+            ab = _bits(a[:r])
+            t0 = time.time()
+            aq, as_ = O.quant(ab)
+            O.gemm_ref(aq, as_, bq, bs)
+            ts.append(time.time() - t0)
+        per_row = max(0.0, (ts[1] - ts[0]) / (r2 - r1))
+        fixed = max(0.0, ts[0] - per_row * r1)
+        full = fixed + per_row * wl.m
+        t_full += full
+        per_k[f"k{k}"] = {"sample_s": {str(r1): ts[0], str(r2): ts[1]},
+                          "rows_per_s_marginal": (1.0 / per_row) if per_row > 0 else None,
+                          "fixed_s": fixed, "quant_gemm_s_full_extrapolated": full,
+                          "gemm_gflops_at_sample": gemm_flops(r2, N_OUT, k) / ts[1] / 1e9}
+    flops = sum(gemm_flops(wl.m, N_OUT, k) for k in ks)
+    blas = _blas_threads()
+    return {"value": flops / t_full / 1e12, "unit": "TFLOP/s", "cores": blas or (os.cpu_count() or 1),
+            "kind": "oracle",
+            "sample": f"norm-quant of all {Mn}x{H} rows measured ({t_norm:.1f} s); quant + GEMM measured on the "
+                      f"first {r1} and {r2} of {wl.m} rows and extrapolated linearly to {wl.m} rows; value = GEMM "
+                      "flops of one step / (measured norm-quant + extrapolated quant + GEMM time)",
+            "norm_quant_full_s": t_norm,
+            "norm_quant_gbs": norm_quant_bytes(Mn) / t_norm / 1e9,
+            "per_k": per_k,
+            "step_s_extrapolated": t_full,
+            "threads": {"norm_quant": 1, "quant": 1, "gemm_blas": blas},
+            "host_cpus": os.cpu_count()}
 
 
 def _oracle_prepare(wl, ks, rows):
     """Untimed: seeded inputs as the oracle takes them, weights quantised by the oracle."""
-    import numpy as np
-    import torch
-
     import oracle as O
-
-    def bits(t):
-        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-
     x, w = wl.norm(seed=0)
     ops = []
     for k in ks:
         a, wt = wl.gemm(k, seed=0)
-        bq, bs = O.quant(bits(wt))
-        ops.append((k, bits(a[:rows]), bq, bs))
-    return {"x": bits(x[:rows]), "w": bits(w), "ops": ops, "rows": rows}
+        bq, bs = O.quant(_bits(wt))
+        ops.append((k, _bits(a[:rows]), bq, bs))
+    return {"x": _bits(x[:rows]), "w": _bits(w), "ops": ops, "rows": rows, "eps": wl.eps}
 
 
 def _oracle_step(prep):
@@ -534,7 +787,7 @@ def _oracle_step(prep):
     of `rows` rows of x, quantisation of `rows` rows of each A, and their GEMM
     rows against the full 6144-row weight.  Returns the GEMM flops done."""
     import oracle as O
-    O.rmsnorm_quant(prep["x"], prep["w"], EPS)
+    O.rmsnorm_quant(prep["x"], prep["w"], prep["eps"])
     flops = 0.0
     for k, ab, bq, bs in prep["ops"]:
         aq, as_ = O.quant(ab)
@@ -543,34 +796,12 @@ def _oracle_step(prep):
     return flops
 
 
-def _sample_text(wl, ks, rows, n, dt):
-    return (f"{n} x ({rows} rows of norm-quant {wl.m}x{H}; {rows} rows of quant + GEMM vs the full "
-            f"6144-row weight for K={list(ks)}), {dt:.1f} s")
-
-
-def cpu_baseline(wl, ks, budget_s=15.0, rows=16):
-    """The oracle timed on a bounded row sample of the step, repeated for about
-    budget_s seconds; reported as TFLOP/s of GEMM work."""
-    prep = _oracle_prepare(wl, ks, rows)
-    flops = 0.0
-    n = 0
-    t0 = time.time()
-    while True:
-        flops += _oracle_step(prep)
-        n += 1
-        if time.time() - t0 >= budget_s:
-            break
-    dt = time.time() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
-            "sample": _sample_text(wl, ks, rows, n, dt)}
-
-
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, each step one bounded sample of the workload."""
     from mxfp8_norm_quant_gb300 import workloads as W
     wl = W.get_workload(args.workload)
     ks = wl.ks
-    rows = 16
+    rows = 64
     prep = _oracle_prepare(wl, ks, rows)
     for _ in range(args.warmup):
         _oracle_step(prep)
@@ -580,16 +811,18 @@ def run_reference(args, rank, world):
         flops += _oracle_step(prep)
     dt = time.time() - t0
     value = flops / dt / 1e12
+    blas = _blas_threads()
+    sample = (f"{args.steps} x ({rows} rows of norm-quant {wl.norm_rows}x{H}; {rows} rows of quant + GEMM vs the "
+              f"full 6144-row weight for K={list(ks)}), {dt:.1f} s")
     return {
         "impl": "reference",
-        "metric": "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144",
+        "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 GEMM of decoded MXFP8, f32 norm", "data": "synthetic",
-        "config": {"workload": wl.name, "M": wl.m, "N": N_OUT, "K": list(ks), "norm_quant": f"{wl.m}x{H}",
-                   "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
-                         "sample": _sample_text(wl, ks, rows, args.steps, dt)},
+        "config": make_config(wl, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas or (os.cpu_count() or 1), "kind": "oracle",
+                         "sample": sample, "threads": {"norm_quant": 1, "quant": 1, "gemm_blas": blas}},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -739,8 +972,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--workload", default="m1024")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--replays", type=int, default=20, help="timed replays of the K-step graph (median reported)")
+    ap.add_argument("--sweep-replays", type=int, default=7, help="timed replays per sweep point")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-config sweep record")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["norm_quant", "norm_rowmajor", "norm_bf16", "swizzle", "quant", "gemm",
                                              "gemm_quant"],
@@ -751,6 +986,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.replays = max(1, args.replays)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

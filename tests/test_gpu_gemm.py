@@ -121,7 +121,8 @@ def test_zero_m_is_noop(cuda_dev):
 def _workload_check(wl, k, dev, n_rows=256, seed=0):
     """The full-size GEMM exactly as bench.py launches it (operands quantised by
     the GPU kernels, which are themselves checked bit-exact elsewhere), checked
-    on a row sample against the oracle."""
+    against the oracle on a row sample, or on every row when n_rows is None
+    (the oracle then runs over row chunks of 4096)."""
     a, wt = wl.gemm(k, seed)
     M, N = a.shape[0], wt.shape[0]
     ad, wd = a.to(dev), wt.to(dev)
@@ -132,9 +133,18 @@ def _workload_check(wl, k, dev, n_rows=256, seed=0):
     torch.cuda.synchronize()
     assert mx.mx_device_fault() == 0
     # operands for the oracle: from the oracle's own quantiser
+    bq_o, bs_o = O.quant(bf16_bits(wt))
+    if n_rows is None or n_rows >= M:
+        worst = 0.0
+        ab = bf16_bits(a)
+        for r in range(0, M, 4096):
+            aq_o, as_o = O.quant(ab[r:r + 4096])
+            ok, w_ = gemm_close(out[r:r + 4096], O.gemm_ref(aq_o, as_o, bq_o, bs_o))
+            assert ok, f"{wl.name} K={k} rows {r}..: worst err/tol = {w_:.3f}"
+            worst = max(worst, w_)
+        return worst
     rng = np.random.default_rng(seed + M + k)
     rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, min(M, n_rows), replace=False)]))
-    bq_o, bs_o = O.quant(bf16_bits(wt))
     aq_o, as_o = O.quant(bf16_bits(a[torch.from_numpy(rows)]))
     ref = O.gemm_ref(aq_o, as_o, bq_o, bs_o)
     ok, worst = gemm_close(out[torch.from_numpy(rows).to(dev)], ref)
@@ -144,14 +154,15 @@ def _workload_check(wl, k, dev, n_rows=256, seed=0):
 
 @pytest.mark.parametrize("name,k", [("m128", 2048), ("m1024", 2048), ("m1024", 3072), ("m4096_rowscale", 2048),
                                     ("m4096_rowscale", 3072), ("m32768_stress", 3072)])
-def test_workload_full_size_sampled(cuda_dev, name, k):
-    _workload_check(W.WORKLOADS[name], k, cuda_dev)
+def test_workload_full_size_every_element(cuda_dev, name, k):
+    _workload_check(W.WORKLOADS[name], k, cuda_dev, n_rows=None)
 
 
 @pytest.mark.parametrize("m", W.M_SWEEP)
 @pytest.mark.parametrize("k", [W.K_OPROJ, W.K_DOWN])
-def test_m_sweep_sampled(cuda_dev, m, k):
-    _workload_check(W.sweep_workload(m, k), k, cuda_dev, n_rows=96, seed=1)
+def test_m_sweep(cuda_dev, m, k):
+    # every element up to M = 4096, a 1024-row sample beyond
+    _workload_check(W.sweep_workload(m, k), k, cuda_dev, n_rows=None if m <= 4096 else 1024, seed=1)
 
 
 def test_plan_is_consistent(cuda_dev):

@@ -134,18 +134,20 @@ def test_bf16_norm_degenerate_rows(cuda_dev):
     assert np.array_equal(bf16_bits(y), O.rmsnorm_bf16(bf16_bits(x), bf16_bits(w), 1e-6))
 
 
-def test_sp_forms_full_workload_sampled(cuda_dev):
-    # the 32768 x 6144 norm in both sequence-parallel forms, against the
-    # oracle on a sample of rows spread over the whole launch
+def test_sp_forms_full_workload(cuda_dev):
+    # the 32768 x 6144 norm in both sequence-parallel forms: every row against
+    # the oracle (computed over row chunks), codes, row-major scales and bf16 y
     M, H = 32768, 6144
     x, w = W.norm_inputs(M, H, seed=77)
     xd, wd = x.to(cuda_dev), w.to(cuda_dev)
     q, s = mx.rmsnorm_quant_rowmajor(xd, wd, 1e-6)
     y = mx.rmsnorm_bf16(xd, wd, 1e-6)
     torch.cuda.synchronize()
-    rows = np.unique(np.concatenate([np.arange(0, M, 997), [M - 1]]))
-    xs = bf16_bits(x[torch.from_numpy(rows)])
-    rq, rs = O.mx_quantize_logical(O.gemma_rmsnorm_f32(xs, bf16_bits(w), 1e-6))
-    assert np.array_equal(np_u8(q)[rows], rq)
-    assert np.array_equal(np_u8(s)[rows], rs)
-    assert np.array_equal(bf16_bits(y)[rows], O.rmsnorm_bf16(xs, bf16_bits(w), 1e-6))
+    gq, gs, gy = np_u8(q), np_u8(s), bf16_bits(y)
+    xb, wb = bf16_bits(x), bf16_bits(w)
+    for r in range(0, M, 4096):
+        yf = O.gemma_rmsnorm_f32(xb[r:r + 4096], wb, 1e-6)
+        rq, rs = O.mx_quantize_logical(yf)
+        assert np.array_equal(gq[r:r + 4096], rq), f"codes, rows {r}.."
+        assert np.array_equal(gs[r:r + 4096], rs), f"row-major scales, rows {r}.."
+        assert np.array_equal(gy[r:r + 4096], O.f32_to_bf16_bits(yf)), f"bf16 y, rows {r}.."
