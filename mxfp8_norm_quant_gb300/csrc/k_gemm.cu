@@ -687,6 +687,22 @@ cudaError_t launch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* bq,
 
 }  // namespace
 
+// x [rows][H] bf16 viewed as [rows][H/64][64] (128-byte lines), 128-byte
+// swizzle; a box is box_lines lines of one row.  Used by the row kernels
+// whose lanes read 64-byte runs of a row from shared memory.
+cudaError_t make_row_tensor_map(CUtensorMap* map, const void* x, int rows, int H, int box_lines) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(H / 64), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(H) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_lines), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Tile shapes: tile_m 128 (one CTA) with tile_n 64/128/192, or tile_m 256 (a
 // CTA pair, cta_group::2) with tile_n 128/192.
 bool gemm_tile_supported(int tile_m, int tile_n) {

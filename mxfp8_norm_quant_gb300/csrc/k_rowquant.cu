@@ -3,7 +3,7 @@
 // The norm kernels themselves are in row_common.cuh.
 #include <cstdint>
 
-#include "row_common.cuh"
+#include "row_lb.cuh"
 
 namespace mxk {
 

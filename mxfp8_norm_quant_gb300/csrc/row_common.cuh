@@ -531,56 +531,6 @@ cudaError_t launch_norm(const uint16_t* x, const uint16_t* w, float eps, uint8_t
   return cudaLaunchKernelEx(&la.cfg, kern, x, w, eps, q, sc, M, H);
 }
 
-// Row ownership: a warp owns a run of chunks (at most 24 x 256 elements in
-// registers); rows wider than one warp's run, and rows in launches with few
-// rows per warp, are split over several warps so that more loads are in
-// flight and each warp's chain is shorter.
-template <int FORM>
-cudaError_t dispatch_norm(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                          int num_sms, unsigned int* fault, cudaStream_t stream) {
-  const uint16_t* x = static_cast<const uint16_t*>(xv);
-  const uint16_t* w = static_cast<const uint16_t*>(wv);
-  const int nchunk = (H + 255) / 256;
-  const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
-  const long long rows_per_warp = M / (warps > 0 ? warps : 1);
-  if (nchunk <= 24 && M > warps) {
-    // more than one row per warp: prefetch the next row while computing
-    if (nchunk <= 8) return launch_norm_pf<8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (nchunk <= 16) return launch_norm_pf<16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (nchunk > 16 && nchunk <= 24) {
-    // rows of 4097..6144 elements, at most one row per warp.  A register
-    // kernel is best while its rows fit one round (6 warps per row: 2 rows
-    // per CTA; 3 warps: 5 rows per CTA); past that the prefetching kernel.
-    // Measured on GB300 at H = 6144 (CUDA-graph timing, inputs rotating
-    // beyond L2; swizzled / row-major / bf16 forms, us):
-    //   M = 128: 6 warps per row 3.3 / 3.1 / 2.9, prefetching 5.5 / 6.1 / 4.4;
-    //   M = 704: 3 warps per row 6.3 / 6.0 / 5.9, 6 warps 7.8 / 7.5 / 7.3,
-    //            prefetching 6.9 / 7.6 / 6.2;
-    //   M = 768: 3 warps (two rounds) 8.3 / 7.9 / 7.3, 6 warps 7.9 / 7.5 / 7.4,
-    //            prefetching 7.2 / 7.9 / 6.3;
-    //   M = 1024: prefetching 7.8 / 8.4 / 7.0.
-    if (M >= 896) return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (M > 256 && M <= NormCta<3>::GROUPS * num_sms)
-      return launch_norm<3, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (M > 256 && FORM != OUT_MX_ROWMAJOR)
-      return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm<6, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-  }
-  if (nchunk <= 24 && (M >= 512 || rows_per_warp > 0)) {
-    if (nchunk <= 4) return launch_norm<1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (nchunk <= 8) return launch_norm<1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (nchunk <= 16) return launch_norm<1, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    return launch_norm<1, 24, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-  }
-  // a few hundred rows: split each row over several warps to shorten the chain
-  if (nchunk <= 8) return launch_norm<2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-  if (nchunk <= 24) return launch_norm<6, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-  if (nchunk <= 32) return launch_norm<4, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-  return launch_norm<4, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-}
-
 }  // namespace
 
 }  // namespace mxk

@@ -53,18 +53,54 @@ def test_norm_quant_small(cuda_dev, M, H):
     _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
 
 
-# Row counts at H = 6144 on either side of each kernel choice of the
-# dispatcher on a 152-SM GPU: 6 warps per row (<= 256 rows), 3 warps per row
-# (<= 760), the prefetching kernel (>= 761; the row-major form keeps 6 warps
-# per row below 896), and its reduce-scatter sum of squares (1217-9728 rows).
-# Every variant must give the same bytes.
+# Row counts on either side of each kernel choice of the chunked kernels'
+# dispatcher on a 152-SM GPU, at H = 6112 (a width the lane-block kernels do
+# not take): 6 warps per row (<= 256 rows), 3 warps per row (<= 760), the
+# prefetching kernel (>= 761; the row-major form keeps 6 warps per row below
+# 896), and its reduce-scatter sum of squares (1217-9728 rows).  Every
+# variant must give the same bytes.
 DISPATCH_ROWS = [256, 257, 760, 761, 895, 896, 1216, 1217, 9728, 9729]
 
 
 @pytest.mark.parametrize("M", DISPATCH_ROWS)
 def test_norm_quant_dispatch_boundaries(cuda_dev, M):
-    H = 6144
+    H = 6112
     x, w = W.norm_inputs(M, H, seed=M + 11)
+    rq, rs = O.rmsnorm_quant(bf16_bits(x), bf16_bits(w), 1e-6)
+    _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
+
+
+def lane_block_boundaries(num_sms):
+    """Row counts on both sides of each kernel choice of the lane-block
+    dispatcher (rows of 4097..6144 elements, H % 64 == 0), for this GPU's SM
+    count: <6,1,2> up to 1.7 rows per SM, <3,2,5> to 4.65, <3,2,8> to 8,
+    <3,2,5> to 16, then <3,2,8> and from 64 rows per SM <3,2,6> (the BF16
+    form: <6,1,4> from 40.4 rows per SM)."""
+    s = num_sms
+    rows = []
+    for last in (17 * s // 10, 465 * s // 100, 8 * s, 16 * s, 64 * s - 1, (202 * s - 1) // 5):
+        rows += [last, last + 1]
+    return rows
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_norm_quant_lane_block_boundaries(cuda_dev, i):
+    M = lane_block_boundaries(torch.cuda.get_device_properties(cuda_dev).multi_processor_count)[i]
+    H = 6144
+    x, w = W.norm_inputs(M, H, seed=M + 13, outlier_frac=0.01, zero_block_frac=1 / 128)
+    rq, rs = O.rmsnorm_quant(bf16_bits(x), bf16_bits(w), 1e-6)
+    _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
+
+
+# lane-block kernels at widths whose last 1024-element chunk is partial
+# (4160: 64 elements, and with 6 warps per row a warp with no chunk at all;
+# 5184; 6080) or whole (5120), with ragged 128-row blocks
+LB_SHAPES = [(300, 4160), (1000, 4160), (4000, 4160), (77, 5120), (3000, 5184), (129, 6080), (2000, 6080)]
+
+
+@pytest.mark.parametrize("M,H", LB_SHAPES)
+def test_norm_quant_lane_block_widths(cuda_dev, M, H):
+    x, w = W.norm_inputs(M, H, seed=M * 5 + H)
     rq, rs = O.rmsnorm_quant(bf16_bits(x), bf16_bits(w), 1e-6)
     _assert_same(*_run_norm(x, w, 1e-6, cuda_dev), rq, rs)
 
@@ -76,10 +112,11 @@ def test_quant_small(cuda_dev, M, H):
     _assert_same(*_run_quant(x, cuda_dev), rq, rs)
 
 
-def test_norm_quant_degenerate_rows(cuda_dev):
+@pytest.mark.parametrize("M,H", [(256, 6144), (2000, 6144), (256, 6112), (1000, 4160)])
+def test_norm_quant_degenerate_rows(cuda_dev, M, H):
     # all-zero rows (r = 1/sqrt(eps)), constant rows, huge and tiny magnitudes,
-    # subnormal bf16 inputs, zero blocks, gain w = -1 (y = 0) and w large
-    M, H = 256, 6144
+    # subnormal bf16 inputs, zero blocks, gain w = -1 (y = 0) and w large;
+    # through the lane-block kernels (H = 6144, 4160) and the chunked ones
     x, w = W.norm_inputs(M, H, seed=3)
     x = x.float()
     x[0] = 0.0

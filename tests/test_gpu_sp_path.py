@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 # 152-SM GPU) with ragged 128-row blocks; widths with 1, 5 and 192 scale
 # columns per row
 SHAPES = [(1, 6144), (300, 6144), (720, 6144), (800, 6144), (1024, 6144), (5000, 6144), (77, 160), (640, 2048),
-          (3000, 4096), (2500, 32), (9, 16384)]
+          (3000, 4096), (2500, 32), (9, 16384), (720, 6112), (800, 6112), (1024, 6112), (5000, 6112),
+          (1000, 4160), (3000, 5184)]
 
 
 def _ids(shapes):
@@ -117,6 +118,24 @@ def test_bf16_norm_then_quantise(cuda_dev, M, H):
     torch.cuda.synchronize()
     rq, rs = O.quant(ref)
     assert np.array_equal(np_u8(gq), rq) and np.array_equal(np_u8(gs), rs)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_sp_forms_lane_block_boundaries(cuda_dev, i):
+    # both sequence-parallel forms on either side of each kernel choice of the
+    # lane-block dispatcher (the row counts of test_gpu_rowquant)
+    from test_gpu_rowquant import lane_block_boundaries
+    M = lane_block_boundaries(torch.cuda.get_device_properties(cuda_dev).multi_processor_count)[i]
+    H = 6144
+    x, w = W.norm_inputs(M, H, seed=M + 17)
+    yf = O.gemma_rmsnorm_f32(bf16_bits(x), bf16_bits(w), 1e-6)
+    rq, rs = O.mx_quantize_logical(yf)
+    gq, gs = _norm_rowmajor(x, w, 1e-6, cuda_dev)
+    assert np.array_equal(gq, rq) and np.array_equal(gs, rs)
+    y = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=cuda_dev)
+    mx.mx_rmsnorm_bf16(x.to(cuda_dev), w.to(cuda_dev), 1e-6, y, M, H)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(y), O.f32_to_bf16_bits(yf))
 
 
 def test_bf16_norm_degenerate_rows(cuda_dev):
