@@ -3,7 +3,7 @@
 // The norm kernels themselves are in row_common.cuh.
 #include <cstdint>
 
-#include "row_lb.cuh"
+#include "quant_lb.cuh"
 
 namespace mxk {
 
@@ -174,14 +174,24 @@ cudaError_t launch_quant_g(const uint16_t* x, uint8_t* q, uint8_t* sc, int rows,
 
 }  // namespace
 
-// Chunks per warp task: long tasks (8 chunks, 8 loads in flight per lane)
-// when there are rows to spare, shorter ones when that would leave warps
-// idle.  Measured on GB300 (CUDA-graph timing, inputs rotating beyond L2):
-// 1024 x 2048: 2.9 / 3.0 / 3.9 us with 2 / 4 / 8 chunks per task;
-// 1024 x 3072: 3.9 us with 4 vs 4.4 with 8; 4096 x 3072: 8.8 us with 4 vs 9.1.
+// The lane-block quantiser (one 1024-element chunk per warp task) once a
+// launch has at least 10 such tasks per SM; below that, the chunked kernel,
+// whose 256-element tasks spread a small launch over more SMs.  Same-box
+// timings (CUDA graphs, inputs rotating beyond L2), us per launch, chunked /
+// lane-block with 1, 2, 4 chunks per task:
+//   128 x 2048    1.78 / 2.15  3.10  3.07      512 x 2048   2.29 / 2.40  3.31  3.24
+//   512 x 3072    2.75 / 2.60  3.26  4.13     1024 x 2048   3.04 / 2.84  3.59  3.54
+//   4096 x 3072   8.72 / 8.09  8.26  9.58    32768 x 3072  53.58 / 46.81 49.19 46.87
+//   32768 x 6144 102.49 / 92.07 102.07 93.28
+// Within the chunked kernel, chunks per warp task: long tasks (8 chunks, 8
+// loads in flight per lane) when there are rows to spare, shorter ones when
+// that would leave warps idle (1024 x 2048: 2.9 / 3.0 / 3.9 us with 2 / 4 / 8
+// chunks per task; 1024 x 3072: 3.9 us with 4 vs 4.4 with 8).
 cudaError_t launch_quant(const void* xv, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
                          unsigned int* /*fault*/, cudaStream_t stream) {
   const uint16_t* x = static_cast<const uint16_t*>(xv);
+  if (static_cast<long long>(rows) * ((cols + 1023) / 1024) >= 10LL * num_sms)
+    return launch_quant_lb_g<1>(x, q, sc, rows, cols, num_sms, stream);
   const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
   const long long nchunk = (cols + 255) / 256;
   const auto tasks = [&](long long g) { return static_cast<long long>(rows) * ((nchunk + g - 1) / g); };

@@ -163,6 +163,32 @@ def test_quant_every_bf16_pattern(cuda_dev):
     _assert_same(*_run_quant(xs, cuda_dev), rq, rs)
 
 
+def test_quant_every_bf16_pattern_lane_block(cuda_dev):
+    # every finite bf16 pattern again, tiled into 1536 rows of 1024 elements:
+    # enough 1024-element tasks to take the lane-block quantiser
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = bits[((bits >> 7) & 0xFF) != 0xFF].astype(np.uint16)
+    vals = np.random.default_rng(2).permutation(vals)
+    tiled = np.resize(vals, 1536 * 1024).reshape(1536, 1024)
+    x = torch.from_numpy(tiled.view(np.int16).copy()).view(torch.bfloat16)
+    rq, rs = O.quant(bf16_bits(x))
+    _assert_same(*_run_quant(x, cuda_dev), rq, rs)
+
+
+@pytest.mark.parametrize("K", [2048, 3072, 6144, 1056])
+@pytest.mark.parametrize("side", [0, 1])
+def test_quant_dispatch_boundary(cuda_dev, K, side):
+    # the row counts on both sides of the switch from the chunked quantiser to
+    # the lane-block one (10 tasks of 1024 elements per SM), plus a width
+    # whose last chunk holds one block
+    s = torch.cuda.get_device_properties(cuda_dev).multi_processor_count
+    per_row = -(-K // 1024)
+    M = -(-10 * s // per_row) - 1 + side
+    x = W.normal_bf16((M, K), 1.0, seed=M + K, tag="A")
+    rq, rs = O.quant(bf16_bits(x))
+    _assert_same(*_run_quant(x, cuda_dev), rq, rs)
+
+
 def test_zero_rows_is_noop(cuda_dev):
     q = torch.full((4,), 7, dtype=torch.uint8, device=cuda_dev)
     mx.mx_rmsnorm_quant(q, q, 1e-6, q, q, 0, 64)
