@@ -47,6 +47,7 @@ L2_BYTES = 129 * 1024 * 1024
 FP8_PER_BF16 = 2.0        # dense FP8 / dense BF16 tensor rate (4.5 / 2.25 PFLOP/s nominal)
 METRIC = "MXFP8 GEMM TFLOP/s (% FP8 peak) & norm-quant GB/s, M=128-32768, N=6144"
 DEFAULT_WORKLOAD = "m32768_stress"
+NEXT_M = (1024, 4096, 32768)       # sizes at which the sweep also times the forms beyond the main path
 
 
 def load_peaks():
@@ -512,7 +513,34 @@ def run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak):
         gbs = norm_quant_bytes(m) / (us * 1e-6) / 1e9
         norm_pts.append({"M": m, "us": us, "us_min": lo, "us_max": hi, "GB/s": gbs,
                          "frac_hbm": gbs / peaks["hbm_gbs"], "launches_per_replay": n})
-    del x_pool, q_pool, s_pool
+    # ---- the sequence-parallel forms of the norm (row-major scales, BF16 y)
+    # and the standalone swizzle, on the same pool
+    next_pts = []
+    y_pool = torch.empty((pool, H), dtype=torch.bfloat16, device=dev)
+    sw_pool = torch.empty(pool * cp, dtype=torch.uint8, device=dev)
+    for m in NEXT_M:
+        nw = windows(m)
+
+        def lr(i, m=m, nw=nw):
+            r0 = (i % nw) * m
+            mx.mx_rmsnorm_quant_ex(x_pool[r0:r0 + m], w_dev, EPS, q_pool[r0:r0 + m], s_pool[r0 * 192:(r0 + m) * 192],
+                                   m, H, mx.MX_SCALES_ROW_MAJOR, sptr)
+
+        def lb(i, m=m, nw=nw):
+            r0 = (i % nw) * m
+            mx.mx_rmsnorm_bf16(x_pool[r0:r0 + m], w_dev, EPS, y_pool[r0:r0 + m], m, H, sptr)
+
+        def ls(i, m=m, nw=nw):
+            r0 = (i % nw) * m
+            mx.mx_swizzle_scales(s_pool[r0 * 192:(r0 + m) * 192], sw_pool[r0 * cp:(r0 + m) * cp], m, H, sptr)
+        for name, fn, nbytes in (("norm_rowmajor", lr, norm_rowmajor_bytes(m)), ("norm_bf16", lb, norm_bf16_bytes(m)),
+                                 ("swizzle", ls, swizzle_bytes(m))):
+            n = rotation(nbytes)
+            us, lo, hi = per_launch_stats(graph_time(torch, stream, fn, n, reps), n)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            next_pts.append({"kernel": name, "M": m, "us": us, "us_min": lo, "us_max": hi, "GB/s": gbs,
+                             "frac_hbm": gbs / peaks["hbm_gbs"]})
+    del x_pool, q_pool, s_pool, y_pool, sw_pool
     torch.cuda.empty_cache()
 
     # ---- quant + GEMM per K
@@ -532,6 +560,8 @@ def run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak):
         nwq = max(3, min(24, math.ceil(2.2 * L2_BYTES / wbytes)))
         wqs = [wq0] + [(wq0[0].clone(), wq0[1].clone()) for _ in range(nwq - 1)]
         c_pool = torch.empty((pool, N_OUT), dtype=torch.bfloat16, device=dev)
+        cq_pool = torch.empty((pool, N_OUT), dtype=torch.uint8, device=dev)
+        cs_pool = torch.empty(pool * cp, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
         for m in W.M_SWEEP:
             nw = windows(m)
@@ -557,7 +587,19 @@ def run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak):
                              "gemm_tflops": tf, "frac_fp8": tf / fp8_peak,
                              "tile": [plan["tile_m"], plan["tile_n"]],
                              "quant_us": qus, "quant_gbs": qgbs, "quant_frac_hbm": qgbs / peaks["hbm_gbs"]})
-        del a_pool, aq_pool, as_pool, wqs, wq0, c_pool
+            if m in NEXT_M:
+                # the GEMM whose epilogue emits C as MXFP8 (codes + F8_128x4 scales)
+                def lgq(i, m=m, nw=nw):
+                    r0 = (i % nw) * m
+                    wq_ = wqs[i % nwq]
+                    mx.mx_gemm_quant(aq_pool[r0:r0 + m], as_pool[r0 * cpk:(r0 + m) * cpk], wq_[0], wq_[1],
+                                     cq_pool[r0:r0 + m], cs_pool[r0 * cp:(r0 + m) * cp], m, N_OUT, k, 0, 0, sptr)
+                n = rotation(gemm_bytes(m, N_OUT, k))
+                gus, glo, ghi = per_launch_stats(graph_time(torch, stream, lgq, n, reps), n)
+                gtf = gemm_flops(m, N_OUT, k) / (gus * 1e-6) / 1e12
+                next_pts.append({"kernel": "gemm_quant", "M": m, "K": k, "us": gus, "us_min": glo, "us_max": ghi,
+                                 "TFLOP/s": gtf, "frac_fp8": gtf / fp8_peak})
+        del a_pool, aq_pool, as_pool, wqs, wq0, c_pool, cq_pool, cs_pool
         torch.cuda.empty_cache()
 
     # ---- m4096_rowscale: LogUniform row scales on A and x
@@ -613,7 +655,10 @@ def run_sweep(args, mx, torch, dev, stream, peaks, fp8_peak):
                     "us = median per launch (min, max over replays)",
             "peaks": {"fp8_tflops": fp8_peak, "hbm_gbs": peaks["hbm_gbs"],
                       "source": f"{peaks['source']}; FP8 = bf16 x {FP8_PER_BF16}"},
-            "gemm_quant": gemm_pts, "norm_quant": norm_pts, "m4096_rowscale": rs}
+            "gemm_quant": gemm_pts, "norm_quant": norm_pts, "m4096_rowscale": rs,
+            "next": {"note": "the rows beyond the main path: the MXFP8-output GEMM (automatic tile), the norm with "
+                             "row-major scales and in BF16, and the standalone F8_128x4 swizzle of row-major scales",
+                     "points": next_pts}}
 
 
 def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):

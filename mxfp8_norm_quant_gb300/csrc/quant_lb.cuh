@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(QLB_THREADS, G <= 2 ? 2 : 1)
       for (int j = 0; j < 4; ++j) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(&v[g][j]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[k])), fabsf(bf16hi(w[k]))));
+        for (int k = 0; k < 4; ++k) amax = max_abs2(amax, bf16lo(w[k]), bf16hi(w[k]));
       }
       const uint32_t byte = ue8m0_from_amax(amax);
       const float2 iv = make_float2(inv_scale_from_ue8m0(byte), inv_scale_from_ue8m0(byte));
@@ -83,8 +83,8 @@ __global__ void __launch_bounds__(QLB_THREADS, G <= 2 ? 2 : 1)
         const float2 t1 = __fmul2_rn(make_float2(bf16lo(w[1]), bf16hi(w[1])), iv);
         const float2 t2 = __fmul2_rn(make_float2(bf16lo(w[2]), bf16hi(w[2])), iv);
         const float2 t3 = __fmul2_rn(make_float2(bf16lo(w[3]), bf16hi(w[3])), iv);
-        codes[2 * j] = cvt_e4m3x2(t0.x, t0.y) | (cvt_e4m3x2(t1.x, t1.y) << 16);
-        codes[2 * j + 1] = cvt_e4m3x2(t2.x, t2.y) | (cvt_e4m3x2(t3.x, t3.y) << 16);
+        codes[2 * j] = cvt_e4m3x4(t0.x, t0.y, t1.x, t1.y);
+        codes[2 * j + 1] = cvt_e4m3x4(t2.x, t2.y, t3.x, t3.y);
       }
       if (b < blocks) stg256(q + static_cast<size_t>(row) * cols + static_cast<size_t>(b) * 32, codes, out32 != 0);
       // a block past the row's end inside the last 4-column group is padding (0)

@@ -293,6 +293,13 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     const float ms = __fdiv_rn(ss, static_cast<float>(H));
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     const float2 rr = make_float2(r, r);
+    // this lane's output addresses in chunk 0 of the row; chunk c adds 1024
+    // codes (2048 bytes of y), 32 row-major scale bytes, or 8 scale words
+    // (4096 bytes) of the F8_128x4 layout
+    uint8_t* q_row = q + (static_cast<size_t>(row) * H + lane * 32) * (FORM == OUT_BF16 ? 2 : 1);
+    uint8_t* sc_row = nullptr;
+    if constexpr (FORM == OUT_MX_ROWMAJOR) sc_row = sc + static_cast<size_t>(row) * blocks + lane;
+    if constexpr (FORM == OUT_MX_SWIZZLED) sc_row = sc + scale_word_off(row, lane >> 2, words) + (lane & 3);
 
     // pass 2: y = (x * r) * (1 + w) block by block, then the output form
 #pragma unroll
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
           uint32_t o[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) o[k] = pack_bf16x2(y[k].x, y[k].y);
-          uint8_t* dst = q + (static_cast<size_t>(row) * H + static_cast<size_t>(b) * 32) * 2;
+          uint8_t* dst = q_row + cg * 2048;
           const uint32_t lo[8] = {o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]};
           const uint32_t hi[8] = {o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]};
           stg256(dst, lo, out32 != 0);
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       } else {
         float amax = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fmaxf(fabsf(y[k].x), fabsf(y[k].y)));
+        for (int k = 0; k < 16; ++k) amax = max_abs2(amax, y[k].x, y[k].y);
         const uint32_t byte = ue8m0_from_amax(amax);
         const float inv = inv_scale_from_ue8m0(byte);
         const float2 iv = make_float2(inv, inv);
@@ -333,15 +340,14 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float2 t0 = __fmul2_rn(y[2 * k], iv), t1 = __fmul2_rn(y[2 * k + 1], iv);
-          codes[k] = cvt_e4m3x2(t0.x, t0.y) | (cvt_e4m3x2(t1.x, t1.y) << 16);
+          codes[k] = cvt_e4m3x4(t0.x, t0.y, t1.x, t1.y);
         }
-        if (b < blocks) stg256(q + static_cast<size_t>(row) * H + static_cast<size_t>(b) * 32, codes, out32 != 0);
+        if (b < blocks) stg256(q_row + cg * 1024, codes, out32 != 0);
         if constexpr (FORM == OUT_MX_ROWMAJOR) {
-          if (b < blocks) sc[static_cast<size_t>(row) * blocks + b] = static_cast<uint8_t>(byte);
+          if (b < blocks) sc_row[cg * 32] = static_cast<uint8_t>(byte);
         } else {
           // a block past the row's end inside the last 4-column group is padding (0)
-          if (b < 4 * words)
-            sc[scale_word_off(row, b >> 2, words) + (b & 3)] = b < blocks ? static_cast<uint8_t>(byte) : uint8_t{0};
+          if (b < 4 * words) sc_row[cg * 8 * 512] = b < blocks ? static_cast<uint8_t>(byte) : uint8_t{0};
         }
       }
     }

@@ -139,7 +139,10 @@ def test_codes_16_byte_aligned_only(cuda_dev):
 
 
 @pytest.mark.parametrize("name,k", [("m1024", 3072), ("m4096_rowscale", 2048), ("m32768_stress", 3072)])
-def test_workload_full_size_sampled(cuda_dev, name, k):
+def test_workload_full_size_every_row(cuda_dev, name, k):
+    # the full-size MXFP8-output GEMM, every row against the float64 oracle;
+    # the oracle runs over row chunks of 4096 (a multiple of 128, so each
+    # chunk's swizzled scales are one contiguous span of the full buffer)
     wl = W.WORKLOADS[name]
     a, wt = wl.gemm(k, 0)
     M, N = a.shape[0], wt.shape[0]
@@ -148,12 +151,12 @@ def test_workload_full_size_sampled(cuda_dev, name, k):
     q, s = mx.gemm_quant(aq, as_, bq, bs_)
     torch.cuda.synchronize()
     assert mx.mx_device_fault() == 0
-    rng = np.random.default_rng(M + k)
-    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, min(M, 128), replace=False)]))
+    gq, gs = np_u8(q), np_u8(s)
     bq_o, bs_o = O.quant(bf16_bits(wt))
-    aq_o, as_o = O.quant(bf16_bits(a[torch.from_numpy(rows)]))
-    ref = O.gemm_ref(aq_o, as_o, bq_o, bs_o)
-    # the sampled rows' codes, and their scales gathered into a layout of their own
-    gq = np_u8(q)[rows]
-    sb = O.unswizzle_scales(np_u8(s), M, N // 32)[rows]
-    _check_against_float64(gq, O.swizzle_scales(sb), ref)
+    ab = bf16_bits(a)
+    span = O.scale_bytes(4096, N)
+    for r in range(0, M, 4096):
+        rows = min(4096, M - r)
+        aq_o, as_o = O.quant(ab[r:r + rows])
+        ref = O.gemm_ref(aq_o, as_o, bq_o, bs_o)
+        _check_against_float64(gq[r:r + rows], gs[r // 4096 * span:r // 4096 * span + O.scale_bytes(rows, N)], ref)
