@@ -37,6 +37,35 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(mx.EXPORTED)
 
 
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    # the boundary is a C ABI: the header compiles as C99 with no CUDA or C++
+    # header, and a C caller links against the library and calls entry points
+    # that need no GPU
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "caller.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"mxgemm.h\"\n"
+        "int main(void) {\n"
+        "  if (mx_scale_bytes(130, 6144) != 256u * 192u) return 1;\n"
+        "  if (mx_rmsnorm_quant(0, 0, 1e-6f, 0, 0, 4, 48, 0) != MX_ERR_SHAPE) return 2;\n"
+        "  if (mx_gemm(0, 0, 0, 0, 0, 0, 256, 256, 0) != MX_OK) return 3;\n"
+        "  printf(\"%s %d\\n\", mx_status_string(MX_ERR_ALIGN), mx_version());\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(mx.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER), str(src),
+                        "-o", str(exe), "-L", libdir, "-lmxgemm", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.startswith("MX_ERR_ALIGN")
+
+
 def test_version_and_status_strings(lib):
     assert mx.mx_version() == 100
     for st, name in mx.MX_STATUS.items():
