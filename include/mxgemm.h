@@ -162,7 +162,9 @@ mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s,
 /* mx_gemm with the output tile forced.  (tile_m, tile_n) = (0, 0) picks
  * automatically; otherwise tile_m = 128 (one CTA per tile, tile_n 64, 128 or
  * 192) or tile_m = 256 (a cluster of two CTAs sharing one tcgen05 MMA, each
- * staging half of the B tile; tile_n 128 or 192).  MX_ERR_SHAPE otherwise. */
+ * staging half of the B tile; tile_n 128, 192 or 256 -- the 256-column tile
+ * has one TMEM accumulator, so a CTA's next tile waits for its epilogue).
+ * MX_ERR_SHAPE otherwise. */
 mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s,
                      const uint8_t* b_q, const uint8_t* b_s,
                      void* out, int64_t M, int64_t N, int64_t K,

@@ -77,6 +77,10 @@ constexpr int SF_COLS = 12;  // TMEM columns per stage: 4 for A's scales, 8 for 
 
 template <int BN, bool PAIR>
 struct Cfg {
+  // TMEM accumulators: two (the epilogue of one tile overlaps the main loop
+  // of the next), or one for the 256-column tile, whose two would leave no
+  // TMEM columns for the scales
+  static constexpr int ACCS = BN <= 192 ? 2 : 1;
   static constexpr int TM = PAIR ? 2 * BM : BM;      // output tile rows
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows staged per CTA
   static constexpr int A_BYTES = BM * BK;
@@ -85,7 +89,7 @@ struct Cfg {
   static constexpr int SFB_BYTES = 1024;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGES_SMEM = SMEM_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES_TMEM = (TMEM_COLS - 2 * BN) / SF_COLS;
+  static constexpr int STAGES_TMEM = (TMEM_COLS - ACCS * BN) / SF_COLS;
   static constexpr int STAGES_MIN = STAGES_SMEM < STAGES_TMEM ? STAGES_SMEM : STAGES_TMEM;
   static constexpr int STAGES = STAGES_MIN > 10 ? 10 : STAGES_MIN;
   static constexpr int OFF_A = 0;
@@ -98,9 +102,10 @@ struct Cfg {
   static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_SLOT + 8;
   static constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;  // + slack to align the base to 1 KB
-  static constexpr int TMEM_SF = 2 * BN;
+  static constexpr int TMEM_SF = ACCS * BN;
   static_assert(STAGES >= 3, "pipeline too shallow");
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 192, "tile width");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
+  static_assert(BN <= 192 || PAIR, "the 256-column tile is a CTA pair's");
   static_assert(B_BYTES % 1024 == 0, "B tiles keep the 1 KB swizzle-atom alignment");
 };
 
@@ -372,7 +377,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           *abort_flag = 1;
           break;
         }
-        const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+        const uint32_t acc = C::ACCS == 2 ? (tc & 1u) : 0u;
+        const uint32_t aph = C::ACCS == 2 ? ((tc >> 1) & 1u) : (tc & 1u);
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u, abort_flag, p.wait_ns)) {
           if (*abort_flag == 0) atomicOr(p.fault, FAULT_GEMM_MMA);
           *abort_flag = 1;
@@ -507,7 +513,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int tile = unit; tile < num_tiles; tile += nunits, ++tc) {
       const bool split = tile + nunits >= num_tiles && tile != unit;  // last tile, not the first
       if (helper && !split) continue;
-      const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+      const uint32_t acc = C::ACCS == 2 ? (tc & 1u) : 0u;
+      const uint32_t aph = C::ACCS == 2 ? ((tc >> 1) & 1u) : (tc & 1u);
       // a helper waits until the epilogue warps have reached the last tile:
       // then that tile's phase is the last one bar_tfull completes, and the
       // parity wait cannot be satisfied by an earlier phase.  That wait spans
@@ -707,12 +714,16 @@ cudaError_t make_row_tensor_map(CUtensorMap* map, const void* x, int rows, int H
 // CTA pair, cta_group::2) with tile_n 128/192.
 bool gemm_tile_supported(int tile_m, int tile_n) {
   if (tile_m == 128) return tile_n == 64 || tile_n == 128 || tile_n == 192;
-  if (tile_m == 256) return tile_n == 128 || tile_n == 192;
+  if (tile_m == 256) return tile_n == 128 || tile_n == 192 || tile_n == 256;
   return false;
 }
 
 int gemm_stages(int tile_m, int tile_n) {
-  if (tile_m == 256) return tile_n == 128 ? Cfg<128, true>::STAGES : tile_n == 192 ? Cfg<192, true>::STAGES : 0;
+  if (tile_m == 256)
+    return tile_n == 128   ? Cfg<128, true>::STAGES
+           : tile_n == 192 ? Cfg<192, true>::STAGES
+           : tile_n == 256 ? Cfg<256, true>::STAGES
+                           : 0;
   switch (tile_n) {
     case 64: return Cfg<64, false>::STAGES;
     case 128: return Cfg<128, false>::STAGES;
@@ -735,6 +746,21 @@ void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n) 
     *tile_m = BM;
     *tile_n = 64;
     return;
+  }
+  // the 256 x 256 pair tile has one accumulator, so a CTA's second tile
+  // waits for the first one's epilogue; it pays where its tiles fit one wave
+  // of pairs and the 256 x 192 ones need two (same-box, N = 6144: M = 768,
+  // K = 2048 takes 11.73 us against 14.67 for 256 x 128 and 14.97 for
+  // 256 x 192; K = 3072 14.44 against 18.63 and 19.28; with more tiles than
+  // pairs it is slower: M = 4096, K = 2048 51.8 against 38.1 us)
+  {
+    const long long pairs = num_sms / 2, mt = (M + 255) / 256;
+    const long long t256 = mt * ((N + 255) / 256), t192 = mt * ((N + 191) / 192);
+    if (t256 <= pairs && t192 > pairs) {
+      *tile_m = 256;
+      *tile_n = 256;
+      return;
+    }
   }
   struct Cand {
     int tm, tn;
@@ -764,7 +790,9 @@ void gemm_pick_tile(int M, int N, int K, int num_sms, int* tile_m, int* tile_n) 
 int gemm_grid(int M, int N, int tile_m, int tile_n, int num_sms) {
   if (tile_m == 256) {
     const int tiles = ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
-    const int clusters = tile_n == 128 ? pair_max_clusters<128>(num_sms) : pair_max_clusters<192>(num_sms);
+    const int clusters = tile_n == 128   ? pair_max_clusters<128>(num_sms)
+                         : tile_n == 192 ? pair_max_clusters<192>(num_sms)
+                                         : pair_max_clusters<256>(num_sms);
     return 2 * (tiles < clusters ? tiles : clusters);
   }
   const int tiles = ((M + BM - 1) / BM) * ((N + tile_n - 1) / tile_n);
@@ -785,6 +813,9 @@ cudaError_t dispatch_tile(const uint8_t* aq, const uint8_t* as, const uint8_t* b
                                            wait_ns);
       case 192:
         return launch_tile<192, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
+                                           wait_ns);
+      case 256:
+        return launch_tile<256, true, OUT>(aq, as, bq, bs, out, q, qs, M, N, K, num_sms, fault, stream, withhold,
                                            wait_ns);
       default: return cudaErrorInvalidValue;
     }

@@ -153,7 +153,7 @@ def test_gemm_null_alignment_and_block_n(lib):
         assert _status("mx_gemm", *a, 128, 256, 256, None) == 1
         a[i] = GOOD + 16 * 3 + 8
         assert _status("mx_gemm", *a, 128, 256, 256, None) == 2
-    for tm, tn in ((128, 32), (128, 96), (128, 256), (256, 64), (256, 256), (64, 128), (0, 128), (128, 0)):
+    for tm, tn in ((128, 32), (128, 96), (128, 256), (256, 64), (256, 320), (64, 128), (0, 128), (128, 0)):
         assert _status("mx_gemm_ex", *args, 128, 256, 256, tm, tn, None) == 3
     assert _status("mx_gemm", None, None, None, None, None, 0, 256, 256, None) == 0
 

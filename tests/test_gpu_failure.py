@@ -34,7 +34,7 @@ STALL_BITS = FAULT_GEMM_PRODUCER | FAULT_GEMM_MMA | FAULT_GEMM_EPILOGUE | FAULT_
 
 @pytest.mark.parametrize("M,N,K,tile", [(256, 384, 256, (128, 192)), (256, 384, 256, (128, 64)),
                                         (512, 768, 512, (256, 192)), (4096, 6144, 512, (256, 192)),
-                                        (4096, 6144, 512, (128, 128))])
+                                        (4096, 6144, 512, (128, 128)), (1024, 6144, 256, (256, 256))])
 def test_gemm_stall_gives_up_and_recovers(cuda_dev, M, N, K, tile):
     a, wt = W.gemm_operands(M, K, seed=M + N + K, n=N)
     aq, as_ = O.quant(bf16_bits(a))

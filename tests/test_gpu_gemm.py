@@ -14,7 +14,7 @@ from mxtest import bf16_bits, gemm_close, np_u8, to_dev
 
 pytestmark = pytest.mark.gpu
 
-TILES = [(128, 64), (128, 128), (128, 192), (256, 128), (256, 192)]
+TILES = [(128, 64), (128, 128), (128, 192), (256, 128), (256, 192), (256, 256)]
 
 
 def _tid(t):

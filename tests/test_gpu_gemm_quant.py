@@ -24,7 +24,7 @@ from mxtest import GEMM_RTOL, bf16_bits, np_u8, to_dev
 
 pytestmark = pytest.mark.gpu
 
-TILES = [(128, 64), (128, 128), (128, 192), (256, 128), (256, 192)]
+TILES = [(128, 64), (128, 128), (128, 192), (256, 128), (256, 192), (256, 256)]
 TILE_IDS = [f"{m}x{n}" for m, n in TILES]
 
 
