@@ -82,6 +82,32 @@ __device__ __forceinline__ float block_square_tree(const uint4 (&p)[4]) {
   return __fadd_rn(s[0].x, s[0].y);
 }
 
+// The same tree from the block's values already unpacked as the pairs
+// v[k] = (element k, element k + 16).
+__device__ __forceinline__ float block_square_tree_f(const float2 (&v)[16]) {
+  float2 s[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) s[k] = __fmul2_rn(v[k], v[k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s[k] = __fadd2_rn(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s[k] = __fadd2_rn(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) s[k] = __fadd2_rn(s[2 * k], s[2 * k + 1]);
+  s[0] = __fadd2_rn(s[0], s[1]);
+  return __fadd_rn(s[0].x, s[0].y);
+}
+
+// The pairs (element k, element k + 16), k = 0..15, of a lane's block.
+__device__ __forceinline__ void unpack_block(const uint4 (&p)[4], float2 (&v)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t wl = reinterpret_cast<const uint32_t*>(&p[k >> 3])[(k & 7) >> 1];
+    const uint32_t wh = reinterpret_cast<const uint32_t*>(&p[2 + (k >> 3)])[(k & 7) >> 1];
+    v[k] = (k & 1) ? make_float2(bf16hi(wl), bf16hi(wh)) : make_float2(bf16lo(wl), bf16lo(wh));
+  }
+}
+
 // Byte offset, inside a warp's slot, of piece j (elements 8j..8j+7 of the
 // lane's block) of chunk 0: 128-byte line l/2, 16-byte unit 4(l&1) + j,
 // swizzled by the line index (the TMA 128-byte pattern; slots are 1 KB
@@ -96,6 +122,16 @@ __device__ __forceinline__ uint32_t piece_offset(int lane, int j) {
 // global chunk c: a warp's float4 load of one (c, j, h) is one 512-byte run.
 __device__ __forceinline__ int lb_gain_index(int c, int l, int j, int h) {
   return (((c * 4 + j) * 2 + h) * 32 + l) * 4;
+}
+
+// The gain table for kernels that keep the row unpacked as pairs
+// (element k, element k + 16): float4 q of lane l in chunk c holds the gains
+// of elements 2q, 2q + 16, 2q + 1, 2q + 17 of the lane's block, so a warp's
+// float4 load of one (c, q) is again one 512-byte run.  Element e of the
+// block sits at float (e % 2) * 2 + e / 16 of float4 (e % 16) / 2.
+__device__ __forceinline__ int lb_gain_index_pairs(int c, int l, int e) {
+  const int k = e & 15;
+  return ((c * 8 + (k >> 1)) * 32 + l) * 4 + (k & 1) * 2 + (e >> 4);
 }
 
 template <int WPR, int NCW, int GROUPS>
@@ -116,7 +152,10 @@ struct LbCfg {
 
 // WPR warps per row, NCW 1024-element chunks per warp, GROUPS rows in flight
 // per CTA.  Requires H % 64 == 0 and H <= WPR * NCW * 1024.
-template <int WPR, int NCW, int GROUPS, int FORM>
+// KEEP: the row stays in registers unpacked (twice the registers of the
+// packed row), so pass 2 does not unpack it again: about one instruction per
+// element fewer, for the configurations whose row groups leave the registers.
+template <int WPR, int NCW, int GROUPS, int FORM, bool KEEP>
 __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     k_rmsnorm_lb(const __grid_constant__ CUtensorMap tmap_x, const uint16_t* __restrict__ w, float eps,
                  uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, int out32,
@@ -183,8 +222,14 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       g1.y = in ? __fadd_rn(1.0f, bf16hi(v.z)) : 0.0f;
       g1.z = in ? __fadd_rn(1.0f, bf16lo(v.w)) : 0.0f;
       g1.w = in ? __fadd_rn(1.0f, bf16hi(v.w)) : 0.0f;
-      *reinterpret_cast<float4*>(gains + lb_gain_index(c, l, j, 0)) = g0;
-      *reinterpret_cast<float4*>(gains + lb_gain_index(c, l, j, 1)) = g1;
+      if constexpr (KEEP) {
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) gains[lb_gain_index_pairs(c, l, 8 * j + t)] = g[t];
+      } else {
+        *reinterpret_cast<float4*>(gains + lb_gain_index(c, l, j, 0)) = g0;
+        *reinterpret_cast<float4*>(gains + lb_gain_index(c, l, j, 1)) = g1;
+      }
     }
   }
   __syncthreads();
@@ -222,10 +267,17 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     }
 
     // pass 1: the warp's subtree of squares (chunks beyond the row are zeros)
+    float2 xf[KEEP ? NCW : 1][16];
     float lvl[4];
 #pragma unroll
     for (int c = 0; c < NCW; ++c) {
-      float t = warp_tree(block_square_tree(xv[c]));
+      float t;
+      if constexpr (KEEP) {
+        unpack_block(xv[c], xf[c]);
+        t = warp_tree(block_square_tree_f(xf[c]));
+      } else {
+        t = warp_tree(block_square_tree(xv[c]));
+      }
       int k = 0;
 #pragma unroll
       for (; k < 4; ++k) {
@@ -246,11 +298,18 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       }
     }
     // the row is in registers: the slot may take this warp's part of the next row
+    if constexpr (KEEP) {
 #pragma unroll
-    for (int c = 0; c < NCW; ++c)
+      for (int c = 0; c < NCW; ++c)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        asm volatile("" : "+r"(xv[c][j].x), "+r"(xv[c][j].y), "+r"(xv[c][j].z), "+r"(xv[c][j].w));
+        for (int k = 0; k < 16; ++k) asm volatile("" : "+f"(xf[c][k].x), "+f"(xf[c][k].y));
+    } else {
+#pragma unroll
+      for (int c = 0; c < NCW; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          asm volatile("" : "+r"(xv[c][j].x), "+r"(xv[c][j].y), "+r"(xv[c][j].z), "+r"(xv[c][j].w));
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     const int next = row + stride;
@@ -307,22 +366,37 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       if (c >= nc) break;  // warp-uniform
       const int cg = cw0 + c;
       const int b = cg * 32 + lane;          // this lane's MX block of the row
+      // y[k]: elements (2k, 2k + 1) of the block; with KEEP, (k, k + 16)
       float2 y[16];
+      if constexpr (KEEP) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 ga = *reinterpret_cast<const float4*>(gains + lb_gain_index(cg, lane, j, 0));
-        const float4 gb = *reinterpret_cast<const float4*>(gains + lb_gain_index(cg, lane, j, 1));
-        const uint4 v = xv[c][j];
-        y[4 * j + 0] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr), make_float2(ga.x, ga.y));
-        y[4 * j + 1] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr), make_float2(ga.z, ga.w));
-        y[4 * j + 2] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr), make_float2(gb.x, gb.y));
-        y[4 * j + 3] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr), make_float2(gb.z, gb.w));
+        for (int q = 0; q < 8; ++q) {
+          const float4 g = *reinterpret_cast<const float4*>(gains + ((cg * 8 + q) * 32 + lane) * 4);
+          y[2 * q] = __fmul2_rn(__fmul2_rn(xf[c][2 * q], rr), make_float2(g.x, g.y));
+          y[2 * q + 1] = __fmul2_rn(__fmul2_rn(xf[c][2 * q + 1], rr), make_float2(g.z, g.w));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 ga = *reinterpret_cast<const float4*>(gains + lb_gain_index(cg, lane, j, 0));
+          const float4 gb = *reinterpret_cast<const float4*>(gains + lb_gain_index(cg, lane, j, 1));
+          const uint4 v = xv[c][j];
+          y[4 * j + 0] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), rr), make_float2(ga.x, ga.y));
+          y[4 * j + 1] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), rr), make_float2(ga.z, ga.w));
+          y[4 * j + 2] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), rr), make_float2(gb.x, gb.y));
+          y[4 * j + 3] = __fmul2_rn(__fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), rr), make_float2(gb.z, gb.w));
+        }
       }
+      // element e of the block: y[e / 2] component e % 2, or with KEEP y[e % 16] component e / 16
+      auto elem = [&](int e) -> float {
+        if constexpr (KEEP) return (e < 16) ? y[e].x : y[e - 16].y;
+        return (e & 1) ? y[e >> 1].y : y[e >> 1].x;
+      };
       if constexpr (FORM == OUT_BF16) {
         if (b < blocks) {
           uint32_t o[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = pack_bf16x2(y[k].x, y[k].y);
+          for (int k = 0; k < 16; ++k) o[k] = pack_bf16x2(elem(2 * k), elem(2 * k + 1));
           uint8_t* dst = q_row + cg * 2048;
           const uint32_t lo[8] = {o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]};
           const uint32_t hi[8] = {o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]};
@@ -336,12 +410,11 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
         const uint32_t byte = ue8m0_from_amax(amax);
         const float inv = inv_scale_from_ue8m0(byte);
         const float2 iv = make_float2(inv, inv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) y[k] = __fmul2_rn(y[k], iv);
         uint32_t codes[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 t0 = __fmul2_rn(y[2 * k], iv), t1 = __fmul2_rn(y[2 * k + 1], iv);
-          codes[k] = cvt_e4m3x4(t0.x, t0.y, t1.x, t1.y);
-        }
+        for (int w = 0; w < 8; ++w) codes[w] = cvt_e4m3x4(elem(4 * w), elem(4 * w + 1), elem(4 * w + 2), elem(4 * w + 3));
         if (b < blocks) stg256(q_row + cg * 1024, codes, out32 != 0);
         if constexpr (FORM == OUT_MX_ROWMAJOR) {
           if (b < blocks) sc_row[cg * 32] = static_cast<uint8_t>(byte);
@@ -354,14 +427,14 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
   }
 }
 
-template <int WPR, int NCW, int GROUPS, int FORM>
+template <int WPR, int NCW, int GROUPS, int FORM, bool KEEP = false>
 cudaError_t launch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                            int num_sms, unsigned int* fault, cudaStream_t stream) {
   using C = LbCfg<WPR, NCW, GROUPS>;
   CUtensorMap tmap;
   cudaError_t err = make_row_tensor_map(&tmap, x, M, H, NCW * 16);
   if (err != cudaSuccess) return err;
-  auto kern = k_rmsnorm_lb<WPR, NCW, GROUPS, FORM>;
+  auto kern = k_rmsnorm_lb<WPR, NCW, GROUPS, FORM, KEEP>;
   err = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM);
   if (err != cudaSuccess) return err;
   const int Mw = FORM == OUT_MX_SWIZZLED ? ((M + 127) / 128) * 128 : M;
@@ -447,17 +520,23 @@ cudaError_t dispatch_norm_chunked(const void* xv, const void* wv, float eps, uin
 template <int FORM>
 cudaError_t dispatch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                              int num_sms, unsigned int* fault, cudaStream_t stream) {
+  // The quantising forms keep the row unpacked where the row groups leave the
+  // registers for it (<3,2,5> and <3,2,6>: 5 % fewer instructions at 32768
+  // rows, 63.4 M -> 60.2 M; same-box time equal unthrottled, 1-2 % faster at
+  // 1024-2048 rows); the BF16 form keeps it packed (<3,2,6> would spill).
+  constexpr bool KEEP = FORM != OUT_BF16;
   const long long m10 = 10LL * M, s = num_sms;
   if (m10 <= 17 * s) return launch_norm_lb<6, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (100LL * M <= 465 * s) return launch_norm_lb<3, 2, 5, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  if (100LL * M <= 465 * s)
+    return launch_norm_lb<3, 2, 5, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
   if (M <= 8 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (M <= 16 * s) return launch_norm_lb<3, 2, 5, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  if (M <= 16 * s) return launch_norm_lb<3, 2, 5, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
   if constexpr (FORM == OUT_BF16) {
     if (5LL * M < 202 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
     return launch_norm_lb<6, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
   } else {
     if (M < 64 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<3, 2, 6, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<3, 2, 6, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
   }
 }
 
