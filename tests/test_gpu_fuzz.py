@@ -76,3 +76,43 @@ def test_fuzz_quant(cuda_dev, M, H):
     assert mx.mx_device_fault() == 0
     assert np.array_equal(np_u8(q), rq)
     assert np.array_equal(np_u8(s), rs)
+
+
+def _gemm_shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    tiles = [(0, 0), (128, 64), (128, 128), (128, 192), (256, 128), (256, 192), (256, 256)]
+    out = []
+    for _ in range(n):
+        m = int(rng.integers(1, 700))
+        nn = int(rng.integers(1, 200)) * 32           # N % 32 == 0, so the MXFP8 output form applies too
+        k = int(rng.integers(1, 80)) * 32             # K tails that are not a multiple of 128
+        out.append((m, nn, k, tiles[int(rng.integers(0, len(tiles)))]))
+    return out
+
+
+GEMM_SHAPES = _gemm_shapes(77, 20)
+
+
+@pytest.mark.parametrize("M,N,K,tile", GEMM_SHAPES, ids=[f"{m}x{n}x{k}-{t[0]}x{t[1]}" for m, n, k, t in GEMM_SHAPES])
+def test_fuzz_gemm(cuda_dev, M, N, K, tile):
+    # random shapes: ragged M and N tiles and K tails, every tile; the bf16
+    # output against the float64 oracle within the GEMM tolerance, and the
+    # MXFP8 output equal to the quantiser applied to that bf16 output
+    from mxtest import gemm_close
+    a, wt = W.gemm_operands(M, K, seed=M + 3 * N + 7 * K, n=N)
+    aq, as_ = O.quant(bf16_bits(a))
+    bq, bs_ = O.quant(bf16_bits(wt))
+    d = [torch.from_numpy(np.ascontiguousarray(t)).to(cuda_dev) for t in (aq, as_, bq, bs_)]
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=cuda_dev)
+    mx.mx_gemm_ex(*d, out, M, N, K, *tile)
+    q = torch.full((M, N), 0xA5, dtype=torch.uint8, device=cuda_dev)
+    s = torch.full((mx.mx_scale_bytes(M, N),), 0xA5, dtype=torch.uint8, device=cuda_dev)
+    mx.mx_gemm_quant(*d, q, s, M, N, K, *tile)
+    cq, cs = mx.quant(out)
+    torch.cuda.synchronize()
+    assert mx.mx_device_fault() == 0
+    ok, worst = gemm_close(out, O.gemm_ref(aq, as_, bq, bs_))
+    assert ok, f"worst err/tol = {worst:.3f}"
+    if tile != (0, 0):
+        # the same tile's accumulators: the fused epilogue equals the plain quantiser
+        assert torch.equal(q, cq) and torch.equal(s, cs)
