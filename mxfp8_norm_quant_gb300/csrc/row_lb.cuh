@@ -146,8 +146,8 @@ struct LbCfg {
   static constexpr int OFF_RED = OFF_BARS + WARPS * 8;
   static constexpr int SMEM = OFF_RED + GROUPS * 2 * WPR * 8 + 1024;   // + slack to align the base to 1 KB
   static_assert(WPR == 1 || (NCW & (NCW - 1)) == 0, "multi-warp rows need power-of-two chunk runs");
-  static_assert(WPR == 1 || WPR == 2 || WPR == 3 || WPR == 4 || WPR == 6, "warps per row");
-  static_assert(GROUPS <= 15, "one named barrier per row group");
+  static_assert(WPR == 1 || WPR == 2 || WPR == 3 || WPR == 4 || WPR == 6 || WPR == 8, "warps per row");
+  static_assert(WPR == 1 || GROUPS <= 15, "one named barrier per row group");
 };
 
 // WPR warps per row, NCW 1024-element chunks per warp, GROUPS rows in flight
@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       if constexpr (WPR == 4) ss = __fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3]));
       if constexpr (WPR == 6)
         ss = __fadd_rn(__fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3])), __fadd_rn(t[4], t[5]));
+      if constexpr (WPR == 8)
+        ss = __fadd_rn(__fadd_rn(__fadd_rn(t[0], t[1]), __fadd_rn(t[2], t[3])),
+                       __fadd_rn(__fadd_rn(t[4], t[5]), __fadd_rn(t[6], t[7])));
 #pragma unroll
       for (int k = 0; k < WPR; ++k) ok = ok && o[k] != 0;
     }
@@ -447,7 +450,8 @@ cudaError_t launch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t*
 }
 
 // The chunked kernels of row_common.cuh, for the widths the lane-block
-// kernels do not take (H % 64 != 0, H <= 4096 or H > 6144).  Row ownership: a
+// kernels do not take (H % 64 != 0) and for rows of at most 512 elements in
+// launches of up to 16 rows per SM.  Row ownership: a
 // warp owns a run of 256-element chunks (at most 24 in registers); rows wider
 // than one warp's run, and rows in launches with few rows per warp, are split
 // over several warps so that more loads are in flight and each warp's chain
@@ -540,13 +544,94 @@ cudaError_t dispatch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_
   }
 }
 
-// Rows of 4097..6144 elements (H % 64 == 0, the width of the pages' models)
-// go to the lane-block kernels above; other widths to the chunked kernels.
+// Kernel choice for the other widths the lane-block kernels take (H % 64 ==
+// 0, up to 4096 and 6145..16384 elements), by width class and rows per SM,
+// from same-box timings on 152 SMs (CUDA graphs of launches cycling over more
+// than 2x L2 of input; us per launch, swizzled form, the chunked kernels of
+// row_common.cuh in brackets; the row-major form follows the swizzled one):
+//   H = 256..512: chunked up to 16 rows per SM; 4096 rows <1,1,32> 3.41
+//       (3.74), 16384 rows 8.55 (9.79) at H = 256
+//   H = 1024: 128 rows <1,1,8> 2.03 (2.43); 2048 <1,1,16> 3.11 (3.79);
+//       16384 <1,1,32> 10.4 (13.3)
+//   H = 2048: 512 rows <2,1,4> 2.70 (3.07); 1024 <2,1,8> 3.27 (3.80);
+//       2048 <1,2,16> 4.42 (5.47); 16384 <1,2,24> 17.3 (19.3)
+//   H = 2112 / 3072 (three chunks; WPR = 3 is balanced there): 512 rows
+//       <3,1,4> 2.87 / 3.07 (3.53 / 4.26); 1024 <3,1,8> 3.71 / 4.11;
+//       16384 <1,4,16> 21.6 / 24.9 (23.8 / 27.9)
+//   H = 3136 / 4096: 128 rows <4,1,2> 2.42 / 2.48 (2.84 / 3.29); 2048
+//       <2,2,8> 6.30 / 6.62 (7.99 / 8.85); 16384 <1,4,12> 26.0 / 32.9
+//       (29.2 / 34.2)
+//   H = 7168 / 8192: 128 rows <8,1,2> 2.90 / 3.03 (4.10 / 3.95); 2048
+//       <4,2,4> 10.3 / 11.1 (16.2 / 17.0); 16384 <4,2,6> 53.1 / 63.5
+//       (89.8 / 91.6)
+//   H = 8256 / 12288 / 16384: 512 rows <8,2,2> 5.92 / 6.77 / 7.74 (8.77 /
+//       9.85 / 11.0); 16384 <4,4,3> 88.7 / 93.0, <8,2,3> 123 at 16384
+//       (146 / 155 / 165)
+// The BF16 form stores twice the bytes and prefers fewer rows in flight for
+// its largest launches (16384 rows: H = 8192 <4,2,3> 80.6 against <4,2,6>
+// 89.8, chunked 86.3; H = 12288 <8,2,2> 122 against <4,4,3> 135, chunked
+// 129).
+template <int FORM>
+cudaError_t dispatch_norm_lb_other(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M,
+                                   int H, int num_sms, unsigned int* fault, cudaStream_t stream) {
+  const long long m = M, s = num_sms;
+  if (H <= 1024) {
+    if (m > 16 * s) return launch_norm_lb<1, 1, 32, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (H <= 512) return dispatch_norm_chunked<FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 8 * s) return launch_norm_lb<1, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<1, 1, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+  if (H <= 2048) {
+    if (m <= 4 * s) return launch_norm_lb<2, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 8 * s) return launch_norm_lb<2, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 64 * s) return launch_norm_lb<1, 2, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<1, 2, 24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+  if (H <= 3072) {
+    if (m <= 2 * s) return launch_norm_lb<3, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 4 * s) return launch_norm_lb<3, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 8 * s) return launch_norm_lb<3, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<1, 4, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+  if (H <= 4096) {
+    if (m <= 2 * s) return launch_norm_lb<4, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 4 * s) return launch_norm_lb<4, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if (m <= 16 * s) return launch_norm_lb<2, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<1, 4, 12, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+  if (H <= 8192) {
+    if (2 * m <= 3 * s) return launch_norm_lb<8, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    if constexpr (FORM == OUT_BF16) {
+      if (m <= 64 * s) return launch_norm_lb<4, 2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+      return launch_norm_lb<4, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    } else {
+      if (m <= 16 * s) return launch_norm_lb<4, 2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+      return launch_norm_lb<4, 2, 6, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    }
+  }
+  if (m <= 4 * s) return launch_norm_lb<8, 2, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  if constexpr (FORM == OUT_BF16) {
+    if (H <= 9216 || (H <= 12288 && m <= 64 * s))
+      return launch_norm_lb<8, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<8, 2, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  } else {
+    if (H <= 12288) return launch_norm_lb<4, 4, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+    return launch_norm_lb<8, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+  }
+}
+
+// Rows whose width is a multiple of 64 go to the lane-block kernels
+// (4097..6144, the width of the pages' models, with its own table; the other
+// widths by the table above); widths that are an odd multiple of 32 to the
+// chunked kernels.
 template <int FORM>
 cudaError_t dispatch_norm(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                           int num_sms, unsigned int* fault, cudaStream_t stream) {
+  const uint16_t* w = static_cast<const uint16_t*>(wv);
   if (H % 64 == 0 && H > 4096 && H <= 6144)
-    return dispatch_norm_lb<FORM>(xv, static_cast<const uint16_t*>(wv), eps, q, sc, M, H, num_sms, fault, stream);
+    return dispatch_norm_lb<FORM>(xv, w, eps, q, sc, M, H, num_sms, fault, stream);
+  if (H % 64 == 0 && H <= 16384)
+    return dispatch_norm_lb_other<FORM>(xv, w, eps, q, sc, M, H, num_sms, fault, stream);
   return dispatch_norm_chunked<FORM>(xv, wv, eps, q, sc, M, H, num_sms, fault, stream);
 }
 

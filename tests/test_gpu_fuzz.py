@@ -1,8 +1,9 @@
 """Seeded random shapes through every row kernel's dispatcher: the fused norm
 in its three output forms and the plain quantiser, bit-exact against the
-oracle.  Widths are multiples of 32 up to 16384 (both the lane-block kernels'
-range and the chunked kernels'), row counts from 1 to a few thousand, and the
-inputs mix magnitudes, zero blocks and outlier channels."""
+oracle.  Widths are multiples of 32 up to 16384 (multiples of 64 go to the
+lane-block kernels, odd multiples of 32 to the chunked kernels), row counts
+from 1 to a few thousand, and the inputs mix magnitudes, zero blocks and
+outlier channels."""
 
 import numpy as np
 import pytest
@@ -20,7 +21,7 @@ def _shapes(seed, n):
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(n):
-        # half the widths in the lane-block kernels' range (4097..6144, % 64 == 0)
+        # half the widths near the models' width (4097..6144, % 64 == 0)
         if rng.random() < 0.5:
             h = int(rng.integers(65, 97)) * 64
         else:
