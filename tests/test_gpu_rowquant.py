@@ -112,11 +112,13 @@ def test_quant_small(cuda_dev, M, H):
     _assert_same(*_run_quant(x, cuda_dev), rq, rs)
 
 
-@pytest.mark.parametrize("M,H", [(256, 6144), (2000, 6144), (256, 6112), (1000, 4160)])
+@pytest.mark.parametrize("M,H", [(256, 6144), (2000, 6144), (256, 6112), (1000, 4160), (3000, 512), (300, 1024),
+                                 (700, 2048), (200, 3072), (1500, 4096), (300, 8192), (100, 16384)])
 def test_norm_quant_degenerate_rows(cuda_dev, M, H):
     # all-zero rows (r = 1/sqrt(eps)), constant rows, huge and tiny magnitudes,
     # subnormal bf16 inputs, zero blocks, gain w = -1 (y = 0) and w large;
-    # through the lane-block kernels (H = 6144, 4160) and the chunked ones
+    # through the lane-block kernels (H = 6144, 4160 and one configuration of
+    # each other width class) and the chunked ones (H = 6112)
     x, w = W.norm_inputs(M, H, seed=3)
     x = x.float()
     x[0] = 0.0

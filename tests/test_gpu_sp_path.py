@@ -138,8 +138,9 @@ def test_sp_forms_lane_block_boundaries(cuda_dev, i):
     assert np.array_equal(bf16_bits(y), O.f32_to_bf16_bits(yf))
 
 
-def test_bf16_norm_degenerate_rows(cuda_dev):
-    M, H = 64, 6144
+@pytest.mark.parametrize("H", [6144, 1024, 3072, 8192, 16384, 6112])
+def test_bf16_norm_degenerate_rows(cuda_dev, H):
+    M = 64
     x, w = W.norm_inputs(M, H, seed=4)
     x = x.float()
     x[0] = 0.0
