@@ -127,6 +127,25 @@ mx_status mx_rmsnorm_quant_ex(const void* x, const void* w, float eps,
 mx_status mx_rmsnorm_bf16(const void* x, const void* w, float eps, void* out,
                           int64_t M, int64_t H, mx_stream_t stream);
 
+/* Output forms of the norm, for mx_rmsnorm_plan. */
+enum {
+  MX_NORM_SWIZZLED = 0,  /* mx_rmsnorm_quant                                   */
+  MX_NORM_ROW_MAJOR = 1, /* mx_rmsnorm_quant_ex with MX_SCALES_ROW_MAJOR         */
+  MX_NORM_BF16 = 2       /* mx_rmsnorm_bf16                                    */
+};
+
+/* The kernel the norm entry points launch for an M x H input in output form
+ * `form` on a GPU of num_sms SMs; no device is touched, so it answers on a
+ * machine without a GPU.  plan[4] is written: {warps per row, 1024-element
+ * chunks per warp, rows in flight per CTA, 1 if the row stays unpacked in
+ * registers between the sum of squares and the quantisation} for the
+ * lane-block kernels, or {0, 0, 0, 0} for the chunked kernels (which take
+ * odd multiples of 32 and short rows).  M >= 1, H as for mx_rmsnorm_quant,
+ * num_sms >= 1, form one of the above: else MX_ERR_SHAPE; plan NULL:
+ * MX_ERR_NULL.  The rows-per-SM limits of the choice are same-box timings
+ * of every candidate on a 152-SM GB300. */
+mx_status mx_rmsnorm_plan(int64_t M, int64_t H, int form, int num_sms, int plan[4]);
+
 /* Row-major [rows][cols/32] UE8M0 scales -> the F8_128x4 layout
  * (mx_scale_bytes(rows, cols) bytes, padding written as 0), and back.
  * These are the swizzle that runs after the all-gather of row-major scales

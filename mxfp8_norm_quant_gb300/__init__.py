@@ -36,12 +36,17 @@ EXPORTED = (
     "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
     "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
-    "mx_gemm_selftest_stall",
+    "mx_gemm_selftest_stall", "mx_rmsnorm_plan",
 )
 
 # scale layouts of mx_rmsnorm_quant_ex
 MX_SCALES_F8_128X4 = 0
 MX_SCALES_ROW_MAJOR = 1
+
+# output forms of the norm, for mx_rmsnorm_plan
+MX_NORM_SWIZZLED = 0
+MX_NORM_ROW_MAJOR = 1
+MX_NORM_BF16 = 2
 
 
 class MxError(RuntimeError):
@@ -82,6 +87,7 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_quant.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, i64, i64, i64, i32, i32, vp]
     L.mx_gemm_selftest_stall.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, ctypes.c_uint64, vp]
     L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
+    L.mx_rmsnorm_plan.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i32)]
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.mx_last_cuda_error.argtypes = []
@@ -91,7 +97,7 @@ def lib() -> ctypes.CDLL:
     for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
                  "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
                  "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version",
-                 "mx_gemm_selftest_stall"):
+                 "mx_gemm_selftest_stall", "mx_rmsnorm_plan"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -270,6 +276,15 @@ def mx_gemm_plan(M: int, N: int, K: int):
     _check("mx_gemm_plan", lib().mx_gemm_plan(M, N, K, ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(st),
                                               ctypes.byref(gr)))
     return {"tile_m": tm.value, "tile_n": tn.value, "stages": st.value, "grid": gr.value}
+
+
+def mx_rmsnorm_plan(M: int, H: int, form: int, num_sms: int):
+    """(warps per row, chunks per warp, rows per CTA, row kept unpacked) of the
+    lane-block kernel the norm launches, or (0, 0, 0, 0) for the chunked
+    kernels; needs no GPU."""
+    plan = (ctypes.c_int * 4)()
+    _check("mx_rmsnorm_plan", lib().mx_rmsnorm_plan(M, H, form, num_sms, plan))
+    return tuple(int(v) for v in plan)
 
 
 def mx_e4m3_encode_f32(inp, out, n: int, stream=None) -> None:

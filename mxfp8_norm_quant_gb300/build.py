@@ -26,7 +26,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmxgemm.so")
 
 SOURCES = ["k_rowquant.cu", "k_rownorm_sp.cu", "k_rownorm_bf16.cu", "k_gemm.cu", "api.cu"]
-HEADERS = ["mx_ptx.cuh", "mx_kernels.h", "row_common.cuh", "row_lb.cuh", "quant_lb.cuh"]
+HEADERS = ["mx_ptx.cuh", "mx_kernels.h", "norm_plan.h", "row_common.cuh", "row_lb.cuh", "quant_lb.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

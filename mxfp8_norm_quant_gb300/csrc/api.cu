@@ -8,8 +8,13 @@
 
 #include "mx_kernels.h"
 #include "mxgemm.h"
+#include "norm_plan.h"
 
 #define MX_API extern "C" __attribute__((visibility("default")))
+
+static_assert(MX_NORM_SWIZZLED == mxk::OUT_MX_SWIZZLED && MX_NORM_ROW_MAJOR == mxk::OUT_MX_ROWMAJOR &&
+                  MX_NORM_BF16 == mxk::OUT_BF16,
+              "the header's norm forms are the kernels' output forms");
 
 // The library's device fault word.  Kernels that give up a bounded wait set a
 // bit here (see mx_device_fault) instead of hanging the GPU.
@@ -277,6 +282,19 @@ MX_API mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s, const uin
 MX_API mx_status mx_gemm(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q, const uint8_t* b_s, void* out,
                          int64_t M, int64_t N, int64_t K, mx_stream_t stream) {
   return mx_gemm_ex(a_q, a_s, b_q, b_s, out, M, N, K, 0, 0, stream);
+}
+
+MX_API mx_status mx_rmsnorm_plan(int64_t M, int64_t H, int form, int num_sms, int plan[4]) {
+  mx_status st = check_row_op(M, H);
+  if (st != MX_OK) return st;
+  if (M < 1 || num_sms < 1 || form < MX_NORM_SWIZZLED || form > MX_NORM_BF16) return MX_ERR_SHAPE;
+  if (!plan) return MX_ERR_NULL;
+  const mxk::NormPlan pl = mxk::plan_norm(form, M, static_cast<int>(H), num_sms);
+  plan[0] = pl.wpr;
+  plan[1] = pl.ncw;
+  plan[2] = pl.groups;
+  plan[3] = pl.keep;
+  return MX_OK;
 }
 
 MX_API mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m, int* tile_n, int* stages, int* grid) {

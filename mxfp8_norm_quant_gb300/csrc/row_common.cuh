@@ -38,6 +38,7 @@
 
 #include "mx_kernels.h"
 #include "mx_ptx.cuh"
+#include "norm_plan.h"
 
 namespace mxk {
 
@@ -45,13 +46,6 @@ namespace {
 
 constexpr int ROW_WARPS = 16;
 constexpr int ROW_THREADS = ROW_WARPS * 32;
-
-// Output forms of the norm kernels.
-enum RowOutForm : int {
-  OUT_MX_SWIZZLED = 0,  // E4M3 codes + F8_128x4 scales (padding rows zeroed)
-  OUT_MX_ROWMAJOR = 1,  // E4M3 codes + [M][H/32] row-major scales
-  OUT_BF16 = 2,         // the normalised rows rounded to BF16
-};
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;

@@ -502,137 +502,68 @@ cudaError_t dispatch_norm_chunked(const void* xv, const void* wv, float eps, uin
   return launch_norm<4, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
 }
 
-// Kernel choice for rows of 4097..6144 elements (H % 64 == 0), by rows per
-// SM, from same-box timings of the candidates at H = 6144 on 152 SMs (CUDA
-// graphs of launches cycling over inputs larger than 2x L2; us per launch,
-// swizzled form; row-major within 1-4 % of it):
-//   M      <6,1,2> <3,2,5> <3,2,8> <3,2,6>
-//   256     3.22    3.29    3.41    3.39
-//   512     4.60    4.22    4.33    4.30
-//   1024    7.09    6.34    5.89    6.76
-//   1280    8.31    6.88    7.48    7.25
-//   2048   11.11    9.06    9.10    9.83
-//   4096   19.77   14.68   14.16   14.86
-//   8192   36.48   25.49   24.96   25.19
-//   32768 137.46   91.72   97.83   89.66
-// (the chunked kernels of row_common.cuh: 3.23, 5.58, 7.87, 8.66, 10.81,
-// 17.56, 30.56, 101.35).  The BF16 form stores twice the bytes and prefers
-// <6,1,4> from 6144 rows (8192: 31.6 against 33.3 for <3,2,8>; 32768: 118.4
-// against 131.2).  A kernel whose row groups fill the SMs in one round is
-// best while the rows fit; <3,2,5> takes the second round's remainder better
-// between 8 and 16 rows per SM.
+// The lane-block kernel `pl` names (norm_plan.h), for the output form FORM.
+// Every shape the plan can choose for FORM is instantiated here; any other
+// is an error.
 template <int FORM>
-cudaError_t dispatch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                             int num_sms, unsigned int* fault, cudaStream_t stream) {
-  // The quantising forms keep the row unpacked where the row groups leave the
-  // registers for it (<3,2,5> and <3,2,6>: 5 % fewer instructions at 32768
-  // rows, 63.4 M -> 60.2 M; same-box time equal unthrottled, 1-2 % faster at
-  // 1024-2048 rows); the BF16 form keeps it packed (<3,2,6> would spill).
-  constexpr bool KEEP = FORM != OUT_BF16;
-  const long long m10 = 10LL * M, s = num_sms;
-  if (m10 <= 17 * s) return launch_norm_lb<6, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (100LL * M <= 465 * s)
-    return launch_norm_lb<3, 2, 5, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (M <= 8 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (M <= 16 * s) return launch_norm_lb<3, 2, 5, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if constexpr (FORM == OUT_BF16) {
-    if (5LL * M < 202 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<6, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  } else {
-    if (M < 64 * s) return launch_norm_lb<3, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<3, 2, 6, FORM, KEEP>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
+cudaError_t launch_norm_plan(const NormPlan& pl, const void* x, const uint16_t* w, float eps, uint8_t* q,
+                             uint8_t* sc, int M, int H, int num_sms, unsigned int* fault, cudaStream_t stream) {
+  constexpr bool BF = FORM == OUT_BF16;
+#define MX_NORM_CASE(W, N, G, K, FORMS_OK)                                                                   \
+  case norm_plan_key(W, N, G, K):                                                                            \
+    if constexpr (FORMS_OK)                                                                                  \
+      return launch_norm_lb<W, N, G, FORM, (K) != 0>(x, w, eps, q, sc, M, H, num_sms, fault, stream);       \
+    break;
+  switch (norm_plan_key(pl.wpr, pl.ncw, pl.groups, pl.keep)) {
+    // 4097..6144 elements
+    MX_NORM_CASE(6, 1, 2, 0, true)
+    MX_NORM_CASE(3, 2, 5, 1, !BF)
+    MX_NORM_CASE(3, 2, 5, 0, BF)
+    MX_NORM_CASE(3, 2, 8, 0, true)
+    MX_NORM_CASE(3, 2, 6, 1, !BF)
+    MX_NORM_CASE(6, 1, 4, 0, BF)
+    // up to 1024 elements
+    MX_NORM_CASE(1, 1, 8, 0, true)
+    MX_NORM_CASE(1, 1, 16, 0, true)
+    MX_NORM_CASE(1, 1, 32, 0, true)
+    // 1025..2048
+    MX_NORM_CASE(2, 1, 4, 0, true)
+    MX_NORM_CASE(2, 1, 8, 0, true)
+    MX_NORM_CASE(1, 2, 16, 0, true)
+    MX_NORM_CASE(1, 2, 24, 0, true)
+    // 2049..3072
+    MX_NORM_CASE(3, 1, 2, 0, true)
+    MX_NORM_CASE(3, 1, 4, 0, true)
+    MX_NORM_CASE(3, 1, 8, 0, true)
+    MX_NORM_CASE(1, 4, 16, 0, true)
+    // 3073..4096
+    MX_NORM_CASE(4, 1, 2, 0, true)
+    MX_NORM_CASE(4, 1, 4, 0, true)
+    MX_NORM_CASE(2, 2, 8, 0, true)
+    MX_NORM_CASE(1, 4, 12, 0, true)
+    // 6145..8192
+    MX_NORM_CASE(8, 1, 2, 0, true)
+    MX_NORM_CASE(4, 2, 4, 0, true)
+    MX_NORM_CASE(4, 2, 6, 0, !BF)
+    MX_NORM_CASE(4, 2, 3, 0, BF)
+    // 8193..16384
+    MX_NORM_CASE(8, 2, 2, 0, true)
+    MX_NORM_CASE(8, 2, 3, 0, true)
+    MX_NORM_CASE(4, 4, 3, 0, !BF)
+    default: break;
   }
+#undef MX_NORM_CASE
+  return cudaErrorInvalidValue;
 }
 
-// Kernel choice for the other widths the lane-block kernels take (H % 64 ==
-// 0, up to 4096 and 6145..16384 elements), by width class and rows per SM,
-// from same-box timings on 152 SMs (CUDA graphs of launches cycling over more
-// than 2x L2 of input; us per launch, swizzled form, the chunked kernels of
-// row_common.cuh in brackets; the row-major form follows the swizzled one):
-//   H = 256..512: chunked up to 16 rows per SM; 4096 rows <1,1,32> 3.41
-//       (3.74), 16384 rows 8.55 (9.79) at H = 256
-//   H = 1024: 128 rows <1,1,8> 2.03 (2.43); 2048 <1,1,16> 3.11 (3.79);
-//       16384 <1,1,32> 10.4 (13.3)
-//   H = 2048: 512 rows <2,1,4> 2.70 (3.07); 1024 <2,1,8> 3.27 (3.80);
-//       2048 <1,2,16> 4.42 (5.47); 16384 <1,2,24> 17.3 (19.3)
-//   H = 2112 / 3072 (three chunks; WPR = 3 is balanced there): 512 rows
-//       <3,1,4> 2.87 / 3.07 (3.53 / 4.26); 1024 <3,1,8> 3.71 / 4.11;
-//       16384 <1,4,16> 21.6 / 24.9 (23.8 / 27.9)
-//   H = 3136 / 4096: 128 rows <4,1,2> 2.42 / 2.48 (2.84 / 3.29); 2048
-//       <2,2,8> 6.30 / 6.62 (7.99 / 8.85); 16384 <1,4,12> 26.0 / 32.9
-//       (29.2 / 34.2)
-//   H = 7168 / 8192: 128 rows <8,1,2> 2.90 / 3.03 (4.10 / 3.95); 2048
-//       <4,2,4> 10.3 / 11.1 (16.2 / 17.0); 16384 <4,2,6> 53.1 / 63.5
-//       (89.8 / 91.6)
-//   H = 8256 / 12288 / 16384: 512 rows <8,2,2> 5.92 / 6.77 / 7.74 (8.77 /
-//       9.85 / 11.0); 16384 <4,4,3> 88.7 / 93.0, <8,2,3> 123 at 16384
-//       (146 / 155 / 165)
-// The BF16 form stores twice the bytes and prefers fewer rows in flight for
-// its largest launches (16384 rows: H = 8192 <4,2,3> 80.6 against <4,2,6>
-// 89.8, chunked 86.3; H = 12288 <8,2,2> 122 against <4,4,3> 135, chunked
-// 129).
-template <int FORM>
-cudaError_t dispatch_norm_lb_other(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M,
-                                   int H, int num_sms, unsigned int* fault, cudaStream_t stream) {
-  const long long m = M, s = num_sms;
-  if (H <= 1024) {
-    if (m > 16 * s) return launch_norm_lb<1, 1, 32, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (H <= 512) return dispatch_norm_chunked<FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 8 * s) return launch_norm_lb<1, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<1, 1, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (H <= 2048) {
-    if (m <= 4 * s) return launch_norm_lb<2, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 8 * s) return launch_norm_lb<2, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 64 * s) return launch_norm_lb<1, 2, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<1, 2, 24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (H <= 3072) {
-    if (m <= 2 * s) return launch_norm_lb<3, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 4 * s) return launch_norm_lb<3, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 8 * s) return launch_norm_lb<3, 1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<1, 4, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (H <= 4096) {
-    if (m <= 2 * s) return launch_norm_lb<4, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 4 * s) return launch_norm_lb<4, 1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if (m <= 16 * s) return launch_norm_lb<2, 2, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<1, 4, 12, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-  if (H <= 8192) {
-    if (2 * m <= 3 * s) return launch_norm_lb<8, 1, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    if constexpr (FORM == OUT_BF16) {
-      if (m <= 64 * s) return launch_norm_lb<4, 2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-      return launch_norm_lb<4, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    } else {
-      if (m <= 16 * s) return launch_norm_lb<4, 2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-      return launch_norm_lb<4, 2, 6, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    }
-  }
-  if (m <= 4 * s) return launch_norm_lb<8, 2, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if constexpr (FORM == OUT_BF16) {
-    if (H <= 9216 || (H <= 12288 && m <= 64 * s))
-      return launch_norm_lb<8, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<8, 2, 2, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  } else {
-    if (H <= 12288) return launch_norm_lb<4, 4, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-    return launch_norm_lb<8, 2, 3, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
-  }
-}
-
-// Rows whose width is a multiple of 64 go to the lane-block kernels
-// (4097..6144, the width of the pages' models, with its own table; the other
-// widths by the table above); widths that are an odd multiple of 32 to the
-// chunked kernels.
+// The norm in output form FORM: the kernel plan_norm chooses.
 template <int FORM>
 cudaError_t dispatch_norm(const void* xv, const void* wv, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                           int num_sms, unsigned int* fault, cudaStream_t stream) {
-  const uint16_t* w = static_cast<const uint16_t*>(wv);
-  if (H % 64 == 0 && H > 4096 && H <= 6144)
-    return dispatch_norm_lb<FORM>(xv, w, eps, q, sc, M, H, num_sms, fault, stream);
-  if (H % 64 == 0 && H <= 16384)
-    return dispatch_norm_lb_other<FORM>(xv, w, eps, q, sc, M, H, num_sms, fault, stream);
-  return dispatch_norm_chunked<FORM>(xv, wv, eps, q, sc, M, H, num_sms, fault, stream);
+  const NormPlan pl = plan_norm(FORM, M, H, num_sms);
+  if (pl.wpr == 0) return dispatch_norm_chunked<FORM>(xv, wv, eps, q, sc, M, H, num_sms, fault, stream);
+  return launch_norm_plan<FORM>(pl, xv, static_cast<const uint16_t*>(wv), eps, q, sc, M, H, num_sms, fault,
+                                stream);
 }
 
 }  // namespace
