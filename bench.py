@@ -360,15 +360,46 @@ def run_gpu(args, rank, world):
     clocks = sampler.summary(t_soak, t_wall1)
     ms_per_step = statistics.median(replay_ms) / args.steps
 
-    # per-kernel durations: a graph of each kernel's K launches (same
-    # rotating buffers), replayed and timed the same way
     order = ["norm_quant"]
     for k in ks:
         order += [f"quant_a{k}", f"gemm_k{k}"]
-    per_kernel = {}
+    # per-kernel durations inside the step: the same K steps captured again
+    # with a CUDA event on the stream before and after every launch (event
+    # nodes of the graph), replayed; a kernel's time is the sum over the K
+    # steps of its events' interval, per launch, median over replays.  The
+    # events end each kernel's overlap with the next one's set-up, so this
+    # graph runs a little longer than the timed one.
+    ev = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+           for _ in order] for _ in range(args.steps)]
+    g_inst = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_inst, stream=stream):
+        for i in range(args.steps):
+            for idx in range(len(order)):
+                ev[i][idx][0].record(stream)
+                one_kernel(i, idx)
+                ev[i][idx][1].record(stream)
+    n_inst = max(5, args.replays // 2)
+    in_step = {name: [] for name in order}
+    inst_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(n_inst):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_inst.replay()
+            e1.record(stream)
+            stream.synchronize()
+            inst_ms.append(e0.elapsed_time(e1))
+            for idx, name in enumerate(order):
+                in_step[name].append(sum(ev[i][idx][0].elapsed_time(ev[i][idx][1]) for i in range(args.steps)))
+    del g_inst
+    per_kernel = {name: per_launch_stats(t, args.steps) for name, t in in_step.items()}
+    # and each kernel alone: a graph of its K launches (same rotating
+    # buffers), replayed and timed like the step
+    alone = {}
     for idx, name in enumerate(order):
-        t = graph_time(torch, stream, lambda i: one_kernel(i, idx), args.steps, max(5, args.replays // 2))
-        per_kernel[name] = per_launch_stats(t, args.steps)
+        t = graph_time(torch, stream, lambda i: one_kernel(i, idx), args.steps, n_inst)
+        alone[name] = per_launch_stats(t, args.steps)
     sampler.stop()
     assert mx.mx_device_fault() == 0
 
@@ -387,6 +418,8 @@ def run_gpu(args, rank, world):
         else:
             f = gemm_flops(M, N_OUT, int(name[6:]))
             rec.update({"TFLOP/s": f / (us * 1e-6) / 1e12, "frac_fp8": f / (us * 1e-6) / 1e12 / fp8_peak})
+        us_alone = alone[name][0]
+        rec["alone_us"] = us_alone
         kern[name] = rec
     plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
 
@@ -460,8 +493,11 @@ def run_gpu(args, rank, world):
                    "gpu_launches_per_replay": len(order) * args.steps,
                    "rotating_sets": R,
                    "rotating_MiB": round((set_bytes + weight_bytes) * R / 2**20),
-                   "per_kernel": "a CUDA graph of the kernel's K launches (same rotating buffers), "
-                                 "replayed and timed the same way; us = median per launch"},
+                   "per_kernel": "us: inside the step, from CUDA events recorded before and after every "
+                                 "launch of the K-step graph (a second capture of the same steps, replayed "
+                                 f"{n_inst} times; median per launch); alone_us: a CUDA graph of the kernel's K "
+                                 "launches (same rotating buffers), replayed and timed the same way",
+                   "instrumented_ms_per_step": statistics.median(inst_ms) / args.steps},
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
@@ -743,10 +779,42 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     flops = sum(gemm_flops(M, N_OUT, k) for k in ks)
+    # the host link on this machine, with the step's own copies and no compute:
+    # the inputs in on one stream and the outputs out on another, at once
+    b = bufs[0]
+
+    def copies():
+        with torch.cuda.stream(s_in):
+            b["x"].copy_(x_pin, non_blocking=True)
+            for k in ks:
+                b[f"a{k}"].copy_(a_pin[k], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            b["q_h"].copy_(b["q"], non_blocking=True)
+            b["s_h"].copy_(b["s"], non_blocking=True)
+            for k in ks:
+                b[f"c{k}_h"].copy_(b[f"c{k}"], non_blocking=True)
+
+    copies()
+    torch.cuda.synchronize()
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(s_in)
+    s_out.wait_event(l0)
+    n_link = max(3, min(args.steps, 10))
+    for _ in range(n_link):
+        copies()
+    s_out.wait_stream(s_in)
+    l1.record(s_out)
+    torch.cuda.synchronize()
+    link_gbs = n_link * (h2d + d2h) / (l0.elapsed_time(l1) * 1e-3) / 1e9
+    step_gbs = (h2d + d2h) / (ms * 1e-3) / 1e9
     del bufs
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "copy-in, compute and copy-out streams, double-buffered device and pinned host buffers"}
+            "pipeline": "copy-in, compute and copy-out streams, double-buffered device and pinned host buffers",
+            "host_link": {"copies_only_gbs": link_gbs, "step_gbs": step_gbs, "frac": step_gbs / link_gbs,
+                          "what": "the step's own copies (inputs in, outputs out, on two streams at once) "
+                                  "without compute, on this box"}}
 
 
 # ------------------------------------------------------------------ CPU oracle arm
