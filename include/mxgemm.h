@@ -208,6 +208,20 @@ mx_status mx_gemm_quant(const uint8_t* a_q, const uint8_t* a_s,
                         int64_t M, int64_t N, int64_t K,
                         int tile_m, int tile_n, mx_stream_t stream);
 
+/* Self-test of the norm's failure handling.  Launches the lane-block kernel
+ * mx_rmsnorm_quant would launch (H % 64 == 0, else MX_ERR_SHAPE) with its
+ * row copies withheld, so that every warp's bounded wait for a row runs out
+ * after wait_ns nanoseconds (100 us <= wait_ns <= 1 s, else MX_ERR_SHAPE;
+ * M >= 1).  The warps of each row group then stop together and set
+ * FAULT bit 1 (a consumer gave up) in the device fault word (read it with
+ * mx_device_fault); no thread is left waiting.  out_q is not written; scale
+ * bytes of padding rows may be.  Arguments as for mx_rmsnorm_quant.  For
+ * tests only. */
+mx_status mx_rmsnorm_selftest_stall(const void* x, const void* w, float eps,
+                                    uint8_t* out_q, uint8_t* out_scales,
+                                    int64_t M, int64_t H, uint64_t wait_ns,
+                                    mx_stream_t stream);
+
 /* Self-test of the GEMM's failure handling.  Launches mx_gemm_ex's kernel
  * with its producer issuing no copies, so that every bounded wait in it runs
  * out after wait_ns nanoseconds (100 us <= wait_ns <= 1 s, else

@@ -36,7 +36,7 @@ EXPORTED = (
     "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
     "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
-    "mx_gemm_selftest_stall", "mx_rmsnorm_plan",
+    "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall",
 )
 
 # scale layouts of mx_rmsnorm_quant_ex
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_selftest_stall.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, ctypes.c_uint64, vp]
     L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
     L.mx_rmsnorm_plan.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i32)]
+    L.mx_rmsnorm_selftest_stall.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, ctypes.c_uint64, vp]
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.mx_last_cuda_error.argtypes = []
@@ -97,7 +98,7 @@ def lib() -> ctypes.CDLL:
     for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
                  "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
                  "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version",
-                 "mx_gemm_selftest_stall", "mx_rmsnorm_plan"):
+                 "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -269,6 +270,18 @@ def mx_gemm_selftest_stall(a_q, a_s, b_q, b_s, out, M: int, N: int, K: int, tile
     _check("mx_gemm_selftest_stall", lib().mx_gemm_selftest_stall(
         _ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), _ptr(out), M, N, K, tile_m, tile_n, int(wait_ns),
         _stream(stream, a_q)))
+
+
+def mx_rmsnorm_selftest_stall(x, w, eps: float, out_q, out_scales, M: int, H: int, wait_ns: int = 2_000_000,
+                              stream=None) -> None:
+    if _row_shape_ok(M, H):
+        fn = "mx_rmsnorm_selftest_stall"
+        _need(fn, "x", x, 2 * M * H)
+        _need(fn, "w", w, 2 * H)
+        _need(fn, "out_q", out_q, M * H)
+        _need(fn, "out_scales", out_scales, _scale_bytes_py(M, H))
+    _check("mx_rmsnorm_selftest_stall", lib().mx_rmsnorm_selftest_stall(
+        _ptr(x), _ptr(w), float(eps), _ptr(out_q), _ptr(out_scales), M, H, int(wait_ns), _stream(stream, x)))
 
 
 def mx_gemm_plan(M: int, N: int, K: int):

@@ -235,6 +235,23 @@ MX_API mx_status mx_gemm_ex(const uint8_t* a_q, const uint8_t* a_s, const uint8_
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MX_API mx_status mx_rmsnorm_selftest_stall(const void* x, const void* w, float eps, uint8_t* out_q,
+                                           uint8_t* out_scales, int64_t M, int64_t H, uint64_t wait_ns,
+                                           mx_stream_t stream) {
+  mx_status st = check_row_op(M, H);
+  if (st != MX_OK) return st;
+  if (M == 0 || H % 64 != 0 || wait_ns < 100000ull || wait_ns > 1000000000ull) return MX_ERR_SHAPE;
+  if (!x || !w || !out_q || !out_scales) return MX_ERR_NULL;
+  if (misaligned(x) || misaligned(w) || misaligned(out_q) || misaligned(out_scales)) return MX_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = current_device(&d);
+  if (st != MX_OK) return st;
+  if (mxk::plan_norm(MX_NORM_SWIZZLED, M, static_cast<int>(H), d->num_sms).wpr == 0) return MX_ERR_SHAPE;
+  return launched(mxk::launch_rmsnorm_quant_stalled(x, w, eps, out_q, out_scales, static_cast<int>(M),
+                                                    static_cast<int>(H), d->num_sms, d->fault, wait_ns,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MX_API mx_status mx_gemm_selftest_stall(const uint8_t* a_q, const uint8_t* a_s, const uint8_t* b_q,
                                         const uint8_t* b_s, void* out, int64_t M, int64_t N, int64_t K, int tile_m,
                                         int tile_n, uint64_t wait_ns, mx_stream_t stream) {

@@ -142,6 +142,15 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_
   return dispatch_norm<OUT_MX_SWIZZLED>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
 }
 
+cudaError_t launch_rmsnorm_quant_stalled(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M,
+                                         int H, int num_sms, unsigned int* fault, unsigned long long wait_ns,
+                                         cudaStream_t stream) {
+  const NormPlan pl = plan_norm(OUT_MX_SWIZZLED, M, H, num_sms);
+  if (pl.wpr == 0) return cudaErrorInvalidValue;  // the chunked kernels have no row copies to withhold
+  return launch_norm_plan<OUT_MX_SWIZZLED>(pl, x, static_cast<const uint16_t*>(w), eps, q, sc, M, H, num_sms, fault,
+                                           stream, wait_ns, 1);
+}
+
 cudaError_t launch_swizzle_scales(const uint8_t* in, uint8_t* out, int rows, int C, int /*num_sms*/,
                                   cudaStream_t stream) {
   const int smem = 128 * (((C + 3) / 4) * 4 + 4);

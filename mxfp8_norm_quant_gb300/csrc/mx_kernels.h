@@ -41,6 +41,11 @@ struct LaunchAttrs {
 
 cudaError_t launch_rmsnorm_quant(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
                                  int num_sms, unsigned int* fault, cudaStream_t stream);
+// the lane-block norm with its row copies withheld, so that every wait for a
+// row runs out after wait_ns (failure-handling self-test)
+cudaError_t launch_rmsnorm_quant_stalled(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M,
+                                         int H, int num_sms, unsigned int* fault, unsigned long long wait_ns,
+                                         cudaStream_t stream);
 // the same norm with row-major [M][H/32] scales, and with a bf16 [M][H] output
 cudaError_t launch_rmsnorm_quant_rowmajor(const void* x, const void* w, float eps, uint8_t* q, uint8_t* sc, int M,
                                           int H, int num_sms, unsigned int* fault, cudaStream_t stream);

@@ -159,7 +159,7 @@ template <int WPR, int NCW, int GROUPS, int FORM, bool KEEP>
 __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     k_rmsnorm_lb(const __grid_constant__ CUtensorMap tmap_x, const uint16_t* __restrict__ w, float eps,
                  uint8_t* __restrict__ q, uint8_t* __restrict__ sc, int M, int H, int out32,
-                 unsigned int* fault) {
+                 unsigned int* fault, unsigned long long wait_ns, int withhold) {
   using C = LbCfg<WPR, NCW, GROUPS>;
   extern __shared__ uint8_t lb_smem_raw[];
   const uint32_t raw_u32 = smem_u32(lb_smem_raw);
@@ -201,7 +201,9 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
   }
   const int stride = gridDim.x * GROUPS;
   int row = blockIdx.x + gridDim.x * grp;
-  if (lane == 0 && row < M && nc > 0) {
+  // withhold (failure-handling self-test): no row copy is issued, so every
+  // wait for a row runs out after wait_ns
+  if (lane == 0 && row < M && nc > 0 && !withhold) {
     mbar_arrive_expect_tx(bar, C::SLOT);
     tma_load_3d(slot, &tmap_x, 0, cw0 * 16, row, bar);
   }
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     bool ok = true;
     uint4 xv[NCW][4];
     if (nc > 0) {
-      ok = warp_wait(bar, phase, nullptr);
+      ok = warp_wait(bar, phase, nullptr, wait_ns);
       own_ok = ok;
       phase ^= 1u;
 #pragma unroll
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     const int next = row + stride;
-    issued = ok && next < M && nc > 0;
+    issued = ok && next < M && nc > 0 && !withhold;
     if (issued && lane == 0) {
       mbar_arrive_expect_tx(bar, C::SLOT);
       tma_load_3d(slot, &tmap_x, 0, cw0 * 16, next, bar);
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
       // next row's when its own wait succeeded and it issued that copy
       if (lane == 0) {
         atomicOr(fault, FAULT_ROWQ_CONSUMER);
-        if (!own_ok) {
+        if (!own_ok && !withhold) {
           if (!mbar_wait(bar, phase ^ 1u, nullptr, DRAIN_LIMIT_NS)) atomicOr(fault, FAULT_DRAIN);
         } else if (issued) {
           if (!mbar_wait(bar, phase, nullptr, DRAIN_LIMIT_NS)) atomicOr(fault, FAULT_DRAIN);
@@ -432,7 +434,8 @@ __global__ void __launch_bounds__(LbCfg<WPR, NCW, GROUPS>::THREADS, 1)
 
 template <int WPR, int NCW, int GROUPS, int FORM, bool KEEP = false>
 cudaError_t launch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t* q, uint8_t* sc, int M, int H,
-                           int num_sms, unsigned int* fault, cudaStream_t stream) {
+                           int num_sms, unsigned int* fault, cudaStream_t stream,
+                           unsigned long long wait_ns = WAIT_LIMIT_NS, int withhold = 0) {
   using C = LbCfg<WPR, NCW, GROUPS>;
   CUtensorMap tmap;
   cudaError_t err = make_row_tensor_map(&tmap, x, M, H, NCW * 16);
@@ -446,7 +449,7 @@ cudaError_t launch_norm_lb(const void* x, const uint16_t* w, float eps, uint8_t*
   // block offsets are multiples of 32, so the base alone decides
   const int out32 = (reinterpret_cast<uintptr_t>(q) & 31u) == 0 ? 1 : 0;
   LaunchAttrs la(dim3(grid), dim3(C::THREADS), static_cast<size_t>(C::SMEM), stream);
-  return cudaLaunchKernelEx(&la.cfg, kern, tmap, w, eps, q, sc, M, H, out32, fault);
+  return cudaLaunchKernelEx(&la.cfg, kern, tmap, w, eps, q, sc, M, H, out32, fault, wait_ns, withhold);
 }
 
 // The chunked kernels of row_common.cuh, for the widths the lane-block
@@ -507,12 +510,14 @@ cudaError_t dispatch_norm_chunked(const void* xv, const void* wv, float eps, uin
 // is an error.
 template <int FORM>
 cudaError_t launch_norm_plan(const NormPlan& pl, const void* x, const uint16_t* w, float eps, uint8_t* q,
-                             uint8_t* sc, int M, int H, int num_sms, unsigned int* fault, cudaStream_t stream) {
+                             uint8_t* sc, int M, int H, int num_sms, unsigned int* fault, cudaStream_t stream,
+                             unsigned long long wait_ns = WAIT_LIMIT_NS, int withhold = 0) {
   constexpr bool BF = FORM == OUT_BF16;
 #define MX_NORM_CASE(W, N, G, K, FORMS_OK)                                                                   \
   case norm_plan_key(W, N, G, K):                                                                            \
     if constexpr (FORMS_OK)                                                                                  \
-      return launch_norm_lb<W, N, G, FORM, (K) != 0>(x, w, eps, q, sc, M, H, num_sms, fault, stream);       \
+      return launch_norm_lb<W, N, G, FORM, (K) != 0>(x, w, eps, q, sc, M, H, num_sms, fault, stream, wait_ns, \
+                                                     withhold);                                              \
     break;
   switch (norm_plan_key(pl.wpr, pl.ncw, pl.groups, pl.keep)) {
     // 4097..6144 elements

@@ -190,6 +190,24 @@ def test_gemm_selftest_stall_rejects(lib):
         assert _status("mx_gemm_selftest_stall", *a, 128, 256, 256, 0, 0, u64(2_000_000), None) == 2
 
 
+def test_rmsnorm_selftest_stall_rejects(lib):
+    f, u64 = ctypes.c_float(1e-6), ctypes.c_uint64
+    ok_wait = u64(2_000_000)
+    # the wait limit must lie in [100 us, 1 s]; M >= 1; H a multiple of 64 (the
+    # lane-block kernels) within the norm's limits
+    assert _status("mx_rmsnorm_selftest_stall", GOOD, GOOD, f, GOOD, GOOD, 128, 6144, u64(99_999), None) == 3
+    assert _status("mx_rmsnorm_selftest_stall", GOOD, GOOD, f, GOOD, GOOD, 128, 6144, u64(1_000_000_001), None) == 3
+    assert _status("mx_rmsnorm_selftest_stall", GOOD, GOOD, f, GOOD, GOOD, 0, 6144, ok_wait, None) == 3
+    assert _status("mx_rmsnorm_selftest_stall", GOOD, GOOD, f, GOOD, GOOD, 128, 6112, ok_wait, None) == 3
+    assert _status("mx_rmsnorm_selftest_stall", GOOD, GOOD, f, GOOD, GOOD, 128, 16448, ok_wait, None) == 3
+    for i in (0, 1, 3, 4):
+        a = [GOOD, GOOD, f, GOOD, GOOD]
+        a[i] = None
+        assert _status("mx_rmsnorm_selftest_stall", *a, 128, 6144, ok_wait, None) == 1
+        a[i] = GOOD + 8
+        assert _status("mx_rmsnorm_selftest_stall", *a, 128, 6144, ok_wait, None) == 2
+
+
 def test_binding_checks_tensor_buffers(lib):
     # a CPU tensor, or one too small for the call, is refused on the host
     # before its address reaches the library

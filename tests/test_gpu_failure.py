@@ -1,4 +1,4 @@
-"""Failure handling of the GEMM on the GPU, without a broken device.
+"""Failure handling of the GEMM and the norm on the GPU, without a broken device.
 
 Every wait of the GEMM kernel on an mbarrier is bounded: a thread that waits
 longer than the launch's limit sets a bit in the library's device fault word,
@@ -19,11 +19,12 @@ import torch
 import mxfp8_norm_quant_gb300 as mx
 import oracle as O
 from mxfp8_norm_quant_gb300 import workloads as W
-from mxtest import bf16_bits, gemm_close, to_dev
+from mxtest import bf16_bits, gemm_close, np_u8, to_dev
 
 pytestmark = pytest.mark.gpu
 
-# fault bits of the GEMM's bounded waits (the device fault word)
+# fault bits of the bounded waits (the device fault word)
+FAULT_ROWQ_CONSUMER = 1 << 1
 FAULT_GEMM_PRODUCER = 1 << 2
 FAULT_GEMM_MMA = 1 << 3
 FAULT_GEMM_EPILOGUE = 1 << 4
@@ -64,3 +65,31 @@ def test_gemm_stall_gives_up_and_recovers(cuda_dev, M, N, K, tile):
     ok, worst = gemm_close(out2[torch.from_numpy(rows).to(cuda_dev)],
                            O.gemm_ref(aq[rows], O.swizzle_scales(O.unswizzle_scales(as_, M, K // 32)[rows]), bq, bs_))
     assert ok, f"worst err/tol = {worst:.3f}"
+
+
+@pytest.mark.parametrize("M,H", [(128, 6144), (1024, 6144), (2000, 6144), (1000, 4160), (700, 2048), (5000, 8192),
+                                 (300, 16384)])
+def test_norm_stall_gives_up_and_recovers(cuda_dev, M, H):
+    # mx_rmsnorm_selftest_stall withholds the lane-block kernel's row copies:
+    # every warp's wait for its first row runs out, the warps of each row
+    # group stop together, and the call ends within a few limits
+    x, w = W.norm_inputs(M, H, seed=M + H)
+    xd, wd = x.to(cuda_dev), w.to(cuda_dev)
+    torch.cuda.synchronize()
+    assert mx.mx_device_fault() == 0
+    q = torch.full((M, H), 0xA5, dtype=torch.uint8, device=cuda_dev)
+    s = torch.full((mx.mx_scale_bytes(M, H),), 0xA5, dtype=torch.uint8, device=cuda_dev)
+    t0 = time.time()
+    mx.mx_rmsnorm_selftest_stall(xd, wd, 1e-6, q, s, M, H, wait_ns=2_000_000)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    code = mx.mx_device_fault()
+    assert code == FAULT_ROWQ_CONSUMER, f"fault bits {code:#x}"
+    assert elapsed < 2.0, f"the stalled launch took {elapsed:.3f} s"
+    assert bool((q == 0xA5).all()), "a stalled launch wrote codes"
+    # the context is healthy: an ordinary launch is bit-exact
+    mx.mx_rmsnorm_quant(xd, wd, 1e-6, q, s, M, H)
+    torch.cuda.synchronize()
+    assert mx.mx_device_fault() == 0
+    rq, rs = O.rmsnorm_quant(bf16_bits(x), bf16_bits(w), 1e-6)
+    assert np.array_equal(np_u8(q), rq) and np.array_equal(np_u8(s), rs)
