@@ -237,6 +237,13 @@ mx_status mx_gemm_selftest_stall(const uint8_t* a_q, const uint8_t* a_s,
                                  int tile_m, int tile_n, uint64_t wait_ns,
                                  mx_stream_t stream);
 
+/* The output tile mx_gemm chooses for an M x N x K product on a GPU of
+ * num_sms SMs (>= 2); no device is touched, so it answers on a machine
+ * without a GPU.  Shapes as for mx_gemm (else MX_ERR_SHAPE), out-pointers
+ * non-NULL (else MX_ERR_NULL). */
+mx_status mx_gemm_tile_for(int64_t M, int64_t N, int64_t K, int num_sms,
+                           int* tile_m, int* tile_n);
+
 /* The launch configuration mx_gemm would use on the current device: output
  * tile, pipeline stages and grid size (CTAs).  Any out-pointer may be NULL. */
 mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m,

@@ -36,7 +36,7 @@ EXPORTED = (
     "mx_scale_bytes", "mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
     "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
     "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_status_string", "mx_version",
-    "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall",
+    "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall", "mx_gemm_tile_for",
 )
 
 # scale layouts of mx_rmsnorm_quant_ex
@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
     L.mx_gemm_selftest_stall.argtypes = [u8p, u8p, u8p, u8p, vp, i64, i64, i64, i32, i32, ctypes.c_uint64, vp]
     L.mx_gemm_plan.argtypes = [i64, i64, i64] + [ctypes.POINTER(i32)] * 4
     L.mx_rmsnorm_plan.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i32)]
+    L.mx_gemm_tile_for.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     L.mx_rmsnorm_selftest_stall.argtypes = [vp, vp, ctypes.c_float, u8p, u8p, i64, i64, ctypes.c_uint64, vp]
     L.mx_e4m3_encode_f32.argtypes = [vp, u8p, i64, vp]
     L.mx_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -98,7 +99,7 @@ def lib() -> ctypes.CDLL:
     for name in ("mx_rmsnorm_quant", "mx_rmsnorm_quant_ex", "mx_rmsnorm_bf16", "mx_swizzle_scales",
                  "mx_unswizzle_scales", "mx_quant_weights", "mx_gemm", "mx_gemm_ex", "mx_gemm_quant", "mx_gemm_plan",
                  "mx_e4m3_encode_f32", "mx_device_fault", "mx_last_cuda_error", "mx_version",
-                 "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall"):
+                 "mx_gemm_selftest_stall", "mx_rmsnorm_plan", "mx_rmsnorm_selftest_stall", "mx_gemm_tile_for"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -282,6 +283,13 @@ def mx_rmsnorm_selftest_stall(x, w, eps: float, out_q, out_scales, M: int, H: in
         _need(fn, "out_scales", out_scales, _scale_bytes_py(M, H))
     _check("mx_rmsnorm_selftest_stall", lib().mx_rmsnorm_selftest_stall(
         _ptr(x), _ptr(w), float(eps), _ptr(out_q), _ptr(out_scales), M, H, int(wait_ns), _stream(stream, x)))
+
+
+def mx_gemm_tile_for(M: int, N: int, K: int, num_sms: int):
+    """(tile_m, tile_n) mx_gemm chooses on a GPU of num_sms SMs; needs no GPU."""
+    tm, tn = ctypes.c_int(0), ctypes.c_int(0)
+    _check("mx_gemm_tile_for", lib().mx_gemm_tile_for(M, N, K, num_sms, ctypes.byref(tm), ctypes.byref(tn)))
+    return tm.value, tn.value
 
 
 def mx_gemm_plan(M: int, N: int, K: int):

@@ -314,6 +314,15 @@ MX_API mx_status mx_rmsnorm_plan(int64_t M, int64_t H, int form, int num_sms, in
   return MX_OK;
 }
 
+MX_API mx_status mx_gemm_tile_for(int64_t M, int64_t N, int64_t K, int num_sms, int* tile_m, int* tile_n) {
+  mx_status st = check_gemm(M, N, K);
+  if (st != MX_OK) return st;
+  if (num_sms < 2) return MX_ERR_SHAPE;
+  if (!tile_m || !tile_n) return MX_ERR_NULL;
+  mxk::gemm_pick_tile(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), num_sms, tile_m, tile_n);
+  return MX_OK;
+}
+
 MX_API mx_status mx_gemm_plan(int64_t M, int64_t N, int64_t K, int* tile_m, int* tile_n, int* stages, int* grid) {
   mx_status st = check_gemm(M, N, K);
   if (st != MX_OK) return st;
