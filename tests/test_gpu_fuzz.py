@@ -3,7 +3,13 @@ in its three output forms and the plain quantiser, bit-exact against the
 oracle.  Widths are multiples of 32 up to 16384 (multiples of 64 go to the
 lane-block kernels, odd multiples of 32 to the chunked kernels), row counts
 from 1 to a few thousand, and the inputs mix magnitudes, zero blocks and
-outlier channels."""
+outlier channels.
+
+The seeds and the number of shapes can be raised for a longer campaign:
+MX_FUZZ_SEED / MX_FUZZ_N (norm and quantiser shapes, default 2024 / 24) and
+MX_FUZZ_GEMM_SEED / MX_FUZZ_GEMM_N (default 77 / 20)."""
+
+import os
 
 import numpy as np
 import pytest
@@ -31,7 +37,7 @@ def _shapes(seed, n):
     return out
 
 
-SHAPES = _shapes(2024, 24)
+SHAPES = _shapes(int(os.environ.get("MX_FUZZ_SEED", "2024")), int(os.environ.get("MX_FUZZ_N", "24")))
 
 
 def _inputs(m, h, seed):
@@ -91,7 +97,7 @@ def _gemm_shapes(seed, n):
     return out
 
 
-GEMM_SHAPES = _gemm_shapes(77, 20)
+GEMM_SHAPES = _gemm_shapes(int(os.environ.get("MX_FUZZ_GEMM_SEED", "77")), int(os.environ.get("MX_FUZZ_GEMM_N", "20")))
 
 
 @pytest.mark.parametrize("M,N,K,tile", GEMM_SHAPES, ids=[f"{m}x{n}x{k}-{t[0]}x{t[1]}" for m, n, k, t in GEMM_SHAPES])
