@@ -7,15 +7,21 @@
 * A whole step (norm-quant, operand quantisation, GEMM, MXFP8-output GEMM)
   captured in a CUDA graph and replayed must give the bytes the eager calls
   give (the tensor maps are encoded at capture time from the buffers the
-  graph will use)."""
+  graph will use).
+* The norm's output fed straight into a GEMM, and overwritten by the next
+  norm, back to back on one stream: the dependent-launch waits must order
+  each read before the next write."""
 
 import threading
 
+import numpy as np
 import pytest
 import torch
 
 import mxfp8_norm_quant_gb300 as mx
+import oracle as O
 from mxfp8_norm_quant_gb300 import workloads as W
+from mxtest import bf16_bits, gemm_close, np_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -100,3 +106,39 @@ def test_graph_capture_replays_eager_bytes(cuda_dev):
         for got, want in zip(graphed, eager):
             assert torch.equal(got, want)
     assert mx.mx_device_fault() == 0
+
+
+def test_norm_codes_feed_the_gemm_back_to_back(cuda_dev):
+    # the norm's MXFP8 output is the A operand of a GEMM (K = H), and the next
+    # norm overwrites the same q / s while that GEMM may still be reading them:
+    # launched back to back on one stream with no host synchronisation, each
+    # kernel's dependent-launch wait must order the read before the overwrite
+    M, H, N = 640, 6144, 1536
+    st = torch.cuda.Stream(cuda_dev)
+    _, wt = W.gemm_operands(16, H, seed=3, n=N)
+    bq, bs_ = mx.quant(wt.to(cuda_dev))
+    q = torch.empty((M, H), dtype=torch.uint8, device=cuda_dev)
+    s = torch.empty(mx.mx_scale_bytes(M, H), dtype=torch.uint8, device=cuda_dev)
+    xs, ws, cs = [], [], []
+    for i in range(4):
+        x, w = W.norm_inputs(M, H, seed=40 + i, outlier_frac=0.01)
+        xs.append(x)
+        ws.append(w)
+    xd = [x.to(cuda_dev) for x in xs]
+    wd = [w.to(cuda_dev) for w in ws]
+    torch.cuda.synchronize()
+    sp = st.cuda_stream
+    for i in range(4):
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_dev)
+        mx.mx_rmsnorm_quant(xd[i], wd[i], 1e-6, q, s, M, H, sp)
+        mx.mx_gemm(q, s, bq, bs_, c, M, N, H, sp)
+        cs.append(c)
+    st.synchronize()
+    assert mx.mx_device_fault() == 0
+    rows = np.arange(0, M, 5)
+    for i in range(4):
+        rq, rs = O.rmsnorm_quant(bf16_bits(xs[i]), bf16_bits(ws[i]), 1e-6)
+        a_rows = O.swizzle_scales(O.unswizzle_scales(rs, M, H // 32)[rows])
+        ref = O.gemm_ref(rq[rows], a_rows, np_u8(bq), np_u8(bs_))
+        ok, worst = gemm_close(cs[i][torch.from_numpy(rows).to(cuda_dev)], ref)
+        assert ok, f"launch {i}: worst err/tol = {worst:.3f}"
