@@ -192,10 +192,10 @@ cudaError_t launch_quant_g(const uint16_t* x, uint8_t* q, uint8_t* sc, int rows,
 //   512 x 3072    2.75 / 2.60  3.26  4.13     1024 x 2048   3.04 / 2.84  3.59  3.54
 //   4096 x 3072   8.72 / 8.09  8.26  9.58    32768 x 3072  53.58 / 46.81 49.19 46.87
 //   32768 x 6144 102.49 / 92.07 102.07 93.28
-// Within the chunked kernel, chunks per warp task: long tasks (8 chunks, 8
-// loads in flight per lane) when there are rows to spare, shorter ones when
-// that would leave warps idle (1024 x 2048: 2.9 / 3.0 / 3.9 us with 2 / 4 / 8
-// chunks per task; 1024 x 3072: 3.9 us with 4 vs 4.4 with 8).
+// Within the chunked kernel, chunks per warp task: the longest tasks that
+// leave no warp idle (1024 x 2048: 2.9 / 3.0 / 3.9 us with 2 / 4 / 8 chunks
+// per task; 1024 x 3072: 3.9 us with 4 vs 4.4 with 8).  Tasks of 8 chunks
+// would need more than 4 per warp, i.e. launches the lane-block kernel takes.
 cudaError_t launch_quant(const void* xv, uint8_t* q, uint8_t* sc, int rows, int cols, int num_sms,
                          unsigned int* /*fault*/, cudaStream_t stream) {
   const uint16_t* x = static_cast<const uint16_t*>(xv);
@@ -204,7 +204,6 @@ cudaError_t launch_quant(const void* xv, uint8_t* q, uint8_t* sc, int rows, int 
   const long long warps = static_cast<long long>(num_sms) * ROW_WARPS;
   const long long nchunk = (cols + 255) / 256;
   const auto tasks = [&](long long g) { return static_cast<long long>(rows) * ((nchunk + g - 1) / g); };
-  if (tasks(8) >= 4 * warps) return launch_quant_g<8>(x, q, sc, rows, cols, num_sms, stream);
   if (tasks(4) * 5 >= warps * 4) return launch_quant_g<4>(x, q, sc, rows, cols, num_sms, stream);
   if (tasks(2) * 5 >= warps * 4) return launch_quant_g<2>(x, q, sc, rows, cols, num_sms, stream);
   return launch_quant_g<1>(x, q, sc, rows, cols, num_sms, stream);

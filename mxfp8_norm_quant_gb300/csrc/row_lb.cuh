@@ -492,11 +492,11 @@ cudaError_t dispatch_norm_chunked(const void* xv, const void* wv, float eps, uin
       return launch_norm_pf<24, FORM>(x, w, eps, q, sc, M, H, num_sms, fault, stream);
     return launch_norm<6, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
   }
-  if (nchunk <= 24 && (M >= 512 || rows_per_warp > 0)) {
+  // (rows of 17..24 chunks have returned above)
+  if (nchunk <= 16 && (M >= 512 || rows_per_warp > 0)) {
     if (nchunk <= 4) return launch_norm<1, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
     if (nchunk <= 8) return launch_norm<1, 8, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    if (nchunk <= 16) return launch_norm<1, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
-    return launch_norm<1, 24, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
+    return launch_norm<1, 16, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
   }
   // a few hundred rows: split each row over several warps to shorten the chain
   if (nchunk <= 8) return launch_norm<2, 4, FORM>(x, w, eps, q, sc, M, H, num_sms, stream);
