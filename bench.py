@@ -484,7 +484,7 @@ def run_gpu(args, rank, world):
         "norm_quant_roofline": {"bound": "hbm", "achieved": nq["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": nq["frac_hbm"], "peak_source": f"{peaks['source']} HBM copy"},
         "e2e": e2e,
-        "gpu_launches": len(order) * args.steps,
+        "gpu_launches": len(order) * args.steps * args.replays,
         "timing": {"timed_region": f"the K={args.steps}-step CUDA graph, replayed {args.replays} times, each "
                                    "replay timed with CUDA events on the launch stream",
                    "ms_per_step_median": ms_per_step,
