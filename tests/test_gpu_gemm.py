@@ -76,7 +76,9 @@ def test_small_integers_exact(cuda_dev, tile):
 
 
 SHAPES = [(128, 6144, 2048), (1, 96, 32), (300, 416, 288), (129, 256, 4096), (512, 1024, 3072), (77, 6144, 160),
-          (1000, 2016, 1024), (300, 512, 16384)]
+          (1000, 2016, 1024), (300, 512, 16384),
+          # N % 32 == 16: the last 32-column chunk of C is half in the output
+          (200, 48, 256), (130, 6160, 1024), (64, 16, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
