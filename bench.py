@@ -275,9 +275,16 @@ def run_gpu(args, rank, world):
     for k in ks:
         set_bytes += 3 * M * k + mx.mx_scale_bytes(M, k) + 2 * M * N_OUT
     weight_bytes = sum(N_OUT * k + mx.mx_scale_bytes(N_OUT, k) for k in ks)
-    R = max(2, math.ceil(2.2 * L2_BYTES / max(1, set_bytes + weight_bytes)))
-    R = min(R, 16)
     Mn = wl.norm_rows
+    # each kernel alone must also cycle through more than 2.2x L2 of its own
+    # inputs and outputs, so the sets are as many as the smallest kernel needs
+    kernel_bytes = {"norm_quant": norm_quant_bytes(Mn)}
+    for k in ks:
+        kernel_bytes[f"quant_a{k}"] = quant_bytes(M, k)
+        kernel_bytes[f"gemm_k{k}"] = gemm_bytes(M, N_OUT, k)
+    alone_sets = {n: max(1, math.ceil(2.2 * L2_BYTES / b)) for n, b in kernel_bytes.items()}
+    R = max(2, math.ceil(2.2 * L2_BYTES / max(1, set_bytes + weight_bytes)), max(alone_sets.values()))
+    R = min(R, 160)
     sets = []
     for r in range(R):
         s = {"x": x_h.to(dev), "q": torch.empty((Mn, H), dtype=torch.uint8, device=dev),
@@ -393,15 +400,26 @@ def run_gpu(args, rank, world):
             for idx, name in enumerate(order):
                 in_step[name].append(sum(ev[i][idx][0].elapsed_time(ev[i][idx][1]) for i in range(args.steps)))
     del g_inst
-    per_kernel = {name: per_launch_stats(t, args.steps) for name, t in in_step.items()}
+    in_step_stats = {name: per_launch_stats(t, args.steps) for name, t in in_step.items()}
     # and each kernel alone: a graph of its K launches (same rotating
     # buffers), replayed and timed like the step
     alone = {}
     for idx, name in enumerate(order):
-        t = graph_time(torch, stream, lambda i: one_kernel(i, idx), args.steps, n_inst)
-        alone[name] = per_launch_stats(t, args.steps)
+        n_al = min(R, max(args.steps, alone_sets[name]))
+        t = graph_time(torch, stream, lambda i: one_kernel(i, idx), n_al, n_inst)
+        alone[name] = per_launch_stats(t, n_al)
     sampler.stop()
     assert mx.mx_device_fault() == 0
+    # The events cost time of their own (the graph's event nodes delay the
+    # launch after them): the instrumented step minus the step, per launch.
+    # A kernel whose time is not at least 20x that cost is reported alone.
+    inst_ms_per_step = statistics.median(inst_ms) / args.steps
+    event_cost_us = max(0.0, (inst_ms_per_step - ms_per_step) * 1e3 / len(order))
+    per_kernel, timed_how = {}, {}
+    for name in order:
+        in_step_ok = event_cost_us <= 0.05 * in_step_stats[name][0]
+        per_kernel[name] = in_step_stats[name] if in_step_ok else alone[name]
+        timed_how[name] = "in the step" if in_step_ok else "alone"
 
     flops_step = sum(gemm_flops(M, N_OUT, k) for k in ks)
     kern = {}
@@ -418,28 +436,35 @@ def run_gpu(args, rank, world):
         else:
             f = gemm_flops(M, N_OUT, int(name[6:]))
             rec.update({"TFLOP/s": f / (us * 1e-6) / 1e12, "frac_fp8": f / (us * 1e-6) / 1e12 / fp8_peak})
-        us_alone = alone[name][0]
-        rec["alone_us"] = us_alone
+        rec["timed"] = timed_how[name]
+        rec["in_step_us"] = in_step_stats[name][0]
+        rec["alone_us"] = alone[name][0]
         kern[name] = rec
     plan = {k: mx.mx_gemm_plan(M, N_OUT, k) for k in ks}
 
     # the dominant kernel of the step and its roofline
     dom = max(order, key=lambda n: per_kernel[n][0])
     if dom.startswith("gemm_k"):
-        # The kernel is timed inside the long run of the step (the clock
-        # record shows the power cap active), so its denominator is the
-        # sustained measured peak; the burst fraction is reported beside it.
+        # Timed inside the long run of the step (the clock record shows the
+        # power cap active), the kernel's denominator is the sustained
+        # measured peak; timed alone, the burst one.  The burst fraction is
+        # reported beside it either way.
         k = int(dom[6:])
+        in_step = timed_how[dom] == "in the step"
         fp8_sust = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+        peak = fp8_sust if in_step else fp8_peak
         ach = kern[dom]["TFLOP/s"]
-        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_sust, "unit": "TFLOP/s",
-                "frac": ach / fp8_sust, "traffic": gemm_traffic_per_launch(wl.name, k),
+        how = ("sustained bf16 {} TFLOP/s x {} (nominal dense FP8/BF16 ratio), of measured: the kernel is timed "
+               "inside the step's long run under the power cap").format(peaks["bf16_tflops_sustained"], FP8_PER_BF16)
+        if not in_step:
+            how = ("burst bf16 {} TFLOP/s x {} (nominal dense FP8/BF16 ratio), of measured: the kernel is timed "
+                   "alone").format(peaks["bf16_tflops"], FP8_PER_BF16)
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": gemm_traffic_per_launch(wl.name, k),
                 "kernel": f"k_gemm_mxf8, {M}x{N_OUT}x{k}, one launch per step",
                 "algorithmic": {"flops_per_launch": gemm_flops(M, N_OUT, k),
                                 "bytes_per_launch": gemm_bytes(M, N_OUT, k)},
-                "peak_source": f"{peaks['source']} sustained bf16 {peaks['bf16_tflops_sustained']} TFLOP/s x "
-                               f"{FP8_PER_BF16} (nominal dense FP8/BF16 ratio), of measured: the kernel is timed "
-                               "inside the step's long run under the power cap",
+                "peak_source": f"{peaks['source']} {how}",
                 "peak_burst": fp8_peak, "frac_of_burst": ach / fp8_peak}
     else:
         b = norm_quant_bytes(Mn) if dom == "norm_quant" else quant_bytes(M, int(dom[7:]))
@@ -493,11 +518,15 @@ def run_gpu(args, rank, world):
                    "gpu_launches_per_replay": len(order) * args.steps,
                    "rotating_sets": R,
                    "rotating_MiB": round((set_bytes + weight_bytes) * R / 2**20),
-                   "per_kernel": "us: inside the step, from CUDA events recorded before and after every "
-                                 "launch of the K-step graph (a second capture of the same steps, replayed "
-                                 f"{n_inst} times; median per launch); alone_us: a CUDA graph of the kernel's K "
-                                 "launches (same rotating buffers), replayed and timed the same way",
-                   "instrumented_ms_per_step": statistics.median(inst_ms) / args.steps},
+                   "per_kernel": "in_step_us: inside the step, from CUDA events recorded before and after "
+                                 "every launch of the K-step graph (a second capture of the same steps, replayed "
+                                 f"{n_inst} times; median per launch); alone_us: a CUDA graph of max(K, enough "
+                                 "for 2.2x L2 of the kernel's own bytes) launches over the rotating sets, "
+                                 "replayed and timed the same way; us: the "
+                                 "in-step time where the events' own cost per launch (instrumented step minus "
+                                 "step) is at most 5 % of it, else the time alone (`timed` says which)",
+                   "instrumented_ms_per_step": inst_ms_per_step,
+                   "event_cost_us_per_launch": event_cost_us},
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
@@ -781,7 +810,7 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
     flops = sum(gemm_flops(M, N_OUT, k) for k in ks)
     # the host link on this machine, with the step's own copies and no compute:
     # the inputs in on one stream and the outputs out on another, at once;
-    # the best of three trials of five copies each
+    # the best of three trials of at least five copies and 2 GB each
     b = bufs[0]
 
     def copies():
@@ -796,18 +825,19 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
                 b[f"c{k}_h"].copy_(b[f"c{k}"], non_blocking=True)
 
     trials = []
+    n_copies = max(5, math.ceil(2e9 / (h2d + d2h)))
     for _ in range(3):
         torch.cuda.synchronize()
         l0 = torch.cuda.Event(enable_timing=True)
         l1 = torch.cuda.Event(enable_timing=True)
         l0.record(s_in)
         s_out.wait_event(l0)
-        for _ in range(5):
+        for _ in range(n_copies):
             copies()
         s_out.wait_stream(s_in)
         l1.record(s_out)
         torch.cuda.synchronize()
-        trials.append(5 * (h2d + d2h) / (l0.elapsed_time(l1) * 1e-3) / 1e9)
+        trials.append(n_copies * (h2d + d2h) / (l0.elapsed_time(l1) * 1e-3) / 1e9)
     link_gbs = max(trials)
     step_gbs = (h2d + d2h) / (ms * 1e-3) / 1e9
     del bufs
@@ -817,7 +847,8 @@ def run_e2e(args, mx, torch, dev, stream, wl, x_h, w_dev, a_h, wq, ks):
             "host_link": {"copies_only_gbs": link_gbs, "trials_gbs": trials, "step_gbs": step_gbs,
                           "frac": step_gbs / link_gbs,
                           "what": "the step's own copies (inputs in, outputs out, on two streams at once) "
-                                  "without compute, on this box, best of 3 trials of 5; a frac above 1 means the "
+                                  "without compute, on this box, best of 3 trials of max(5, 2 GB) copies; a frac "
+                                  "above 1 means the "
                                   "link was slower during these trials than during the timed steps (the host "
                                   "is shared)"}}
 
