@@ -405,7 +405,7 @@ def run_gpu(args, rank, world):
     # buffers), replayed and timed like the step
     alone = {}
     for idx, name in enumerate(order):
-        n_al = min(R, max(args.steps, alone_sets[name]))
+        n_al = max(args.steps, min(R, alone_sets[name]))
         t = graph_time(torch, stream, lambda i: one_kernel(i, idx), n_al, n_inst)
         alone[name] = per_launch_stats(t, n_al)
     sampler.stop()
